@@ -1,0 +1,116 @@
+"""Seeded synthetic inputs for attention, shared by the oracle and the CUDA path.
+
+This module holds no attention arithmetic: it only draws random tensors with
+torch's CPU generator and rounds them to bfloat16 (round to nearest even), so
+that the oracle (which converts the bf16 values exactly to float64) and the
+CUDA library see the same bytes.
+
+Draw order for one workload: sequence lengths first (variable-length batches
+only), then Q, K, V, dO with ``randn`` in float32 at the packed shape
+``[T, H, d]``, then the per-tensor scale, then the bf16 rounding.
+
+The named workloads are the shapes the tiled-attention pages discuss (dense
+mid-size batches, one long causal sequence, grouped/multi-query heads, and a
+packed variable-length batch) at head dimension 64 or 128.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    causal: bool
+    seed: int
+    N: int = 0                      # sequence length (dense) or max length (varlen)
+    lengths: list | None = None     # per-sequence lengths (varlen), drawn from the seed
+    len_range: tuple | None = None  # (lo, hi) inclusive range for drawn lengths
+    qk_scale: float = 1.0           # Q and K multiplied by this before rounding
+    o_fp32: bool = False            # forward writes an fp32 O
+    deterministic: bool = False     # backward in deterministic mode
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+def workloads() -> dict:
+    """The named workloads, keyed by name."""
+    return {
+        "tiny": Workload("tiny", B=1, Hq=2, Hkv=2, d=64, causal=False, seed=0, N=128,
+                         o_fp32=True),
+        "mid_dense": Workload("mid_dense", B=4, Hq=16, Hkv=16, d=128, causal=False, seed=1,
+                              N=2048),
+        "mid_causal": Workload("mid_causal", B=4, Hq=16, Hkv=16, d=128, causal=True, seed=1,
+                               N=2048),
+        "long_causal": Workload("long_causal", B=1, Hq=16, Hkv=16, d=128, causal=True, seed=2,
+                                N=32768, qk_scale=0.5),
+        "gqa8_causal": Workload("gqa8_causal", B=2, Hq=32, Hkv=8, d=128, causal=True, seed=3,
+                                N=8192),
+        "mqa_causal": Workload("mqa_causal", B=2, Hq=32, Hkv=1, d=128, causal=True, seed=3,
+                               N=8192),
+        "varlen_det": Workload("varlen_det", B=16, Hq=16, Hkv=16, d=128, causal=True, seed=4,
+                               len_range=(256, 8192), deterministic=True),
+    }
+
+
+def draw_lengths(gen: torch.Generator, B: int, lo: int, hi: int) -> list:
+    return [int(x) for x in torch.randint(lo, hi + 1, (B,), generator=gen)]
+
+
+def cu_from_lengths(lengths) -> torch.Tensor:
+    cu = [0]
+    for L in lengths:
+        cu.append(cu[-1] + int(L))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def make_inputs(B, Hq, Hkv, d, seed, N=None, lengths=None, len_range=None, qk_scale=1.0):
+    """Draw (q, k, v, dout, cu_seqlens, lengths) as bf16 CPU tensors.
+
+    Exactly one of N (dense batch of B sequences of length N), lengths
+    (explicit) or len_range (lengths drawn uniformly from [lo, hi]) is used.
+    q, dout: [T, Hq, d]; k, v: [T, Hkv, d]; cu_seqlens: int32 [B+1].
+    """
+    gen = torch.Generator().manual_seed(int(seed))
+    if len_range is not None:
+        lengths = draw_lengths(gen, B, *len_range)
+    elif lengths is None:
+        lengths = [int(N)] * B
+    lengths = [int(x) for x in lengths]
+    T = sum(lengths)
+    q = torch.randn((T, Hq, d), generator=gen, dtype=torch.float32)
+    k = torch.randn((T, Hkv, d), generator=gen, dtype=torch.float32)
+    v = torch.randn((T, Hkv, d), generator=gen, dtype=torch.float32)
+    dout = torch.randn((T, Hq, d), generator=gen, dtype=torch.float32)
+    if qk_scale != 1.0:
+        q = q * qk_scale
+        k = k * qk_scale
+    return dict(
+        q=q.to(torch.bfloat16), k=k.to(torch.bfloat16), v=v.to(torch.bfloat16),
+        dout=dout.to(torch.bfloat16), cu_seqlens=cu_from_lengths(lengths), lengths=lengths)
+
+
+def make_workload(w: Workload, **override):
+    """Inputs for a named workload (fields may be overridden, e.g. N=256)."""
+    kw = dict(B=w.B, Hq=w.Hq, Hkv=w.Hkv, d=w.d, seed=w.seed, qk_scale=w.qk_scale)
+    if w.len_range is not None:
+        kw["len_range"] = w.len_range
+    elif w.lengths is not None:
+        kw["lengths"] = w.lengths
+    else:
+        kw["N"] = w.N
+    kw.update(override)
+    if "N" in override:
+        kw.pop("len_range", None)
+        kw.pop("lengths", None)
+    return make_inputs(**kw)
