@@ -1,0 +1,249 @@
+"""GB300 (sm_103a) tiled exact attention, forward and backward.
+
+Thin Python binding of the C ABI in ``include/fa.h``: every function here
+only marshals arguments (tensors become device pointers, the current torch
+stream becomes the CUDA stream) and calls the shared library built by
+``build.py``; all computation runs in the library's CUDA kernels.  PyTorch is
+used for device memory and streams only.  There is no CPU fallback: if the
+library is missing, or no CUDA device is present, the calls raise.
+
+Layouts (see ``include/fa.h``): q, o, dout, dq ``[T, Hq, d]``; k, v, dk, dv
+``[T, Hkv, d]``; lse, D ``[Hq, T]`` fp32.  A dense batch of B sequences of
+length N is ``T = B*N`` (pass ``cu_seqlens=None``); a packed variable-length
+batch passes ``cu_seqlens`` (int32 ``[B+1]`` on the device) and the maximum
+length N.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "FAError", "lib", "fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_fwd_workspace_size",
+    "fa_bwd_workspace_size", "fa_bwd_workspace_semaphore_offset", "fa_check_device_status",
+    "fa_status_string", "forward", "backward", "attention", "FA_OK", "FA_ERR_INVALID_ARG",
+    "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_BF16", "FA_FP32",
+]
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FA_BF16, FA_FP32 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+_f = ctypes.c_float
+
+_SIGS = {
+    "fa_status_string": (ctypes.c_char_p, [_i]),
+    "fa_version": (ctypes.c_char_p, []),
+    "fa_fwd_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz,
+                    _vp]),
+    "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "fa_bwd_workspace_semaphore_offset": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "fa_bwd_preprocess": (_i, [_vp, _i, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _i, _vp, _i,
+                               _vp]),
+    "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _i, _i, _i, _i, _i,
+                    _i, _f, _i, _vp, _i, _vp]),
+    "fa_check_device_status": (_i, [_vp, _vp]),
+}
+
+EXPORTED = tuple(_SIGS)
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = int(status)
+        super().__init__(f"{what}: {fa_status_string(status)}")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing; build it with "
+                    "`python -m bwd_tiled_attention_gb300.build`")
+            L = ctypes.CDLL(path)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr() if x.numel() > 0 else None
+    return int(x)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dt(dtype) -> int:
+    if isinstance(dtype, int):
+        return dtype
+    if dtype == torch.float32:
+        return FA_FP32
+    if dtype == torch.bfloat16:
+        return FA_BF16
+    raise ValueError(f"unsupported dtype {dtype}")
+
+
+# ----------------------------------------------------------------------------- raw C ABI
+
+
+def fa_status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def fa_fwd_workspace_size(B, Hq, N, total_tokens) -> int:
+    return int(lib().fa_fwd_workspace_size(B, Hq, N, total_tokens))
+
+
+def fa_bwd_workspace_size(B, Hq, Hkv, N, total_tokens, d) -> int:
+    return int(lib().fa_bwd_workspace_size(B, Hq, Hkv, N, total_tokens, d))
+
+
+def fa_bwd_workspace_semaphore_offset(B, Hq, Hkv, N, total_tokens, d) -> int:
+    return int(lib().fa_bwd_workspace_semaphore_offset(B, Hq, Hkv, N, total_tokens, d))
+
+
+def fa_fwd(q, k, v, o, o_dtype, lse, B, Hq, Hkv, N, total_tokens, d, scale, causal, cu_seqlens,
+           workspace, workspace_bytes, stream=None) -> int:
+    return int(lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o_dtype), _ptr(lse), B, Hq,
+                            Hkv, N, total_tokens, d, float(scale), int(bool(causal)),
+                            _ptr(cu_seqlens), _ptr(workspace), int(workspace_bytes),
+                            _stream(stream)))
+
+
+def fa_bwd_preprocess(o, o_dtype, dout, D, workspace, workspace_bytes, B, Hq, Hkv, N,
+                      total_tokens, d, causal, cu_seqlens, deterministic, stream=None) -> int:
+    return int(lib().fa_bwd_preprocess(_ptr(o), _dt(o_dtype), _ptr(dout), _ptr(D),
+                                       _ptr(workspace), int(workspace_bytes), B, Hq, Hkv, N,
+                                       total_tokens, d, int(bool(causal)), _ptr(cu_seqlens),
+                                       int(bool(deterministic)), _stream(stream)))
+
+
+def fa_bwd(q, k, v, dout, lse, D, dq, dk, dv, grad_dtype, workspace, workspace_bytes, B, Hq, Hkv,
+           N, total_tokens, d, scale, causal, cu_seqlens, deterministic, stream=None) -> int:
+    return int(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(D), _ptr(dq),
+                            _ptr(dk), _ptr(dv), _dt(grad_dtype), _ptr(workspace),
+                            int(workspace_bytes), B, Hq, Hkv, N, total_tokens, d, float(scale),
+                            int(bool(causal)), _ptr(cu_seqlens), int(bool(deterministic)),
+                            _stream(stream)))
+
+
+def fa_check_device_status(workspace, stream=None) -> int:
+    return int(lib().fa_check_device_status(_ptr(workspace), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- tensor API
+
+
+def _check(status, what):
+    if status != FA_OK:
+        raise FAError(status, what)
+
+
+def _geometry(q, k, cu_seqlens, max_seqlen, batch):
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if cu_seqlens is None:
+        if batch is None:
+            raise ValueError("dense inputs need batch (B); T = B * N")
+        B = int(batch)
+        N = T // B if B > 0 else 0
+        if B * N != T:
+            raise ValueError("T must equal B * N for a dense batch")
+    else:
+        B = cu_seqlens.numel() - 1
+        if max_seqlen is None:
+            raise ValueError("variable-length inputs need max_seqlen")
+        N = int(max_seqlen)
+    return B, Hq, Hkv, N, T, d
+
+
+def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, max_seqlen=None, batch=None,
+            out_dtype=torch.bfloat16, stream=None, workspace=None):
+    """Attention forward through the C ABI; returns (o, lse)."""
+    B, Hq, Hkv, N, T, d = _geometry(q, k, cu_seqlens, max_seqlen, batch)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty((T, Hq, d), dtype=out_dtype, device=q.device)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    ws_bytes = fa_fwd_workspace_size(B, Hq, N, T)
+    ws = workspace if workspace is not None else torch.empty(
+        max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check(fa_fwd(q, k, v, o, out_dtype, lse, B, Hq, Hkv, N, T, d, scale, causal, cu_seqlens, ws,
+                  ws_bytes, stream), "fa_fwd")
+    return o, lse
+
+
+def backward(q, k, v, o, dout, lse, causal=False, scale=None, cu_seqlens=None, max_seqlen=None,
+             batch=None, deterministic=False, grad_dtype=torch.bfloat16, stream=None,
+             workspace=None, check_status=False):
+    """Attention backward (preprocess + backward) through the C ABI; returns (dq, dk, dv)."""
+    B, Hq, Hkv, N, T, d = _geometry(q, k, cu_seqlens, max_seqlen, batch)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty((T, Hq, d), dtype=grad_dtype, device=q.device)
+    dk = torch.empty((T, Hkv, d), dtype=grad_dtype, device=q.device)
+    dv = torch.empty((T, Hkv, d), dtype=grad_dtype, device=q.device)
+    D = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, N, T, d)
+    ws = workspace if workspace is not None else torch.empty(
+        max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check(fa_bwd_preprocess(o, o.dtype, dout, D, ws, ws_bytes, B, Hq, Hkv, N, T, d, causal,
+                             cu_seqlens, deterministic, stream), "fa_bwd_preprocess")
+    _check(fa_bwd(q, k, v, dout, lse, D, dq, dk, dv, grad_dtype, ws, ws_bytes, B, Hq, Hkv, N, T, d,
+                  scale, causal, cu_seqlens, deterministic, stream), "fa_bwd")
+    if check_status:
+        _check(fa_check_device_status(ws, stream), "fa_bwd (device)")
+    return dq, dk, dv
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale, cu_seqlens, max_seqlen, batch, deterministic):
+        o, lse = forward(q, k, v, causal, scale, cu_seqlens, max_seqlen, batch)
+        ctx.save_for_backward(q, k, v, o, lse, cu_seqlens)
+        ctx.args = (causal, scale, max_seqlen, batch, deterministic)
+        return o
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, o, lse, cu_seqlens = ctx.saved_tensors
+        causal, scale, max_seqlen, batch, deterministic = ctx.args
+        dq, dk, dv = backward(q, k, v, o, dout.contiguous(), lse, causal, scale, cu_seqlens,
+                              max_seqlen, batch, deterministic)
+        return dq, dk, dv, None, None, None, None, None, None
+
+
+def attention(q, k, v, causal=False, scale=None, cu_seqlens=None, max_seqlen=None, batch=None,
+              deterministic=False):
+    """Differentiable attention (autograd wrapper around forward/backward)."""
+    return _Attention.apply(q, k, v, causal, scale, cu_seqlens, max_seqlen, batch, deterministic)

@@ -1,0 +1,278 @@
+// api.cu -- the C ABI declared in include/fa.h: argument validation, TMA
+// tensor-map encoding, workspace layout, and the launch sequence of each call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "common.cuh"
+#include "internal.h"
+
+using namespace fa;
+
+namespace {
+
+constexpr int kMaxVarlenSeqs = 4096;   // scheduler ranks sequences in one CTA
+constexpr int kMaxHeads = 65535;       // head index is packed in 16 bits
+constexpr long long kMaxTiles = 65535; // tile index is packed in 16 bits
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Cached SM count per device.
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// 3-D tensor map over a packed [T, H, d] bf16 array, box {64, 1, 128}, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int T, int H, int d) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kTile};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct Shape {
+    int B, Hq, Hkv, N, T, d;
+    bool varlen;
+};
+
+// Validates the shape arguments shared by every call.  On success fills `s`.
+fa_status check_shape(int B, int Hq, int Hkv, int N, int total_tokens, int d,
+                      const int* cu_seqlens, Shape& s) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || total_tokens < 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (Hq > kMaxHeads) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if ((long long)cdiv(N, kTile) > kMaxTiles) return FA_ERR_UNSUPPORTED;
+    s.B = B; s.Hq = Hq; s.Hkv = Hkv; s.N = N; s.d = d;
+    s.varlen = cu_seqlens != nullptr;
+    if (!s.varlen) {
+        const long long T = (long long)B * N;
+        if (T > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+        if (total_tokens != 0 && total_tokens != T) return FA_ERR_INVALID_ARG;
+        s.T = (int)T;
+    } else {
+        if (B > kMaxVarlenSeqs) return FA_ERR_UNSUPPORTED;
+        if (!aligned4(cu_seqlens)) return FA_ERR_INVALID_ARG;
+        s.T = total_tokens;
+    }
+    if ((long long)s.T * Hq * d > (1LL << 40)) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+const char* fa_version(void) { return "gb300-tiled-attention sm_103a"; }
+
+size_t fa_fwd_workspace_size(int B, int Hq, int N, int total_tokens) {
+    if (B < 0 || Hq <= 0 || N < 0 || total_tokens < 0) return 0;
+    const long long T = total_tokens > 0 ? total_tokens : (long long)B * N;
+    if (T > 0x7FFFFFFFLL) return 0;
+    return fwd_ws_layout(B, Hq, (int)T).bytes;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype,
+                 float* lse, int B, int Hq, int Hkv, int N, int total_tokens, int d, float scale,
+                 int causal, const int* cu_seqlens, void* workspace, size_t workspace_bytes,
+                 fa_stream_t stream) {
+    Shape s;
+    fa_status st = check_shape(B, Hq, Hkv, N, total_tokens, d, cu_seqlens, s);
+    if (st != FA_OK) return st;
+    if (o_dtype != FA_BF16 && o_dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_UNSUPPORTED;
+    if (s.T == 0 || B == 0) return FA_OK;  // nothing to compute
+    if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+        !aligned16(workspace))
+        return FA_ERR_INVALID_ARG;
+    const FwdWs lay = fwd_ws_layout(B, Hq, s.T);
+    if (workspace_bytes < lay.bytes) return FA_ERR_INVALID_ARG;
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!make_map(&p.tm_q, q, s.T, Hq, d) || !make_map(&p.tm_k, k, s.T, Hkv, d) ||
+        !make_map(&p.tm_v, v, s.T, Hkv, d))
+        return FA_ERR_CUDA;
+    p.o = o;
+    p.lse = lse;
+    p.cu_seqlens = cu_seqlens;
+    p.workspace = workspace;
+    p.units_off = lay.units;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.T = s.T; p.d = d;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.causal = causal ? 1 : 0;
+    p.o_fp32 = o_dtype == FA_FP32;
+    const int nsm = sm_count();
+    if (nsm <= 0) return FA_ERR_CUDA;
+    cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_sched(cu_seqlens, B, N, Hq, kFwdBlockRows,
+                                 causal ? kOrderLevelDesc : kOrderSeqDesc, lay.max_units,
+                                 workspace, lay.units, 0, false, strm);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    return cuda_status(launch_fwd(p, nsm, strm));
+}
+
+size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int total_tokens, int d) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || total_tokens < 0 || (d != 64 && d != 128))
+        return 0;
+    const long long T = total_tokens > 0 ? total_tokens : (long long)B * N;
+    if (T > 0x7FFFFFFFLL) return 0;
+    return bwd_ws_layout(B, Hq, Hkv, (int)T, d).bytes;
+}
+
+size_t fa_bwd_workspace_semaphore_offset(int B, int Hq, int Hkv, int N, int total_tokens, int d) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || total_tokens < 0 || (d != 64 && d != 128))
+        return 0;
+    const long long T = total_tokens > 0 ? total_tokens : (long long)B * N;
+    if (T > 0x7FFFFFFFLL) return 0;
+    return bwd_ws_layout(B, Hq, Hkv, (int)T, d).sems;
+}
+
+fa_status fa_bwd_preprocess(const void* o, fa_dtype o_dtype, const void* dout, float* D,
+                            void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                            int N, int total_tokens, int d, int causal,
+                            const int* cu_seqlens, int deterministic, fa_stream_t stream) {
+    Shape s;
+    fa_status st = check_shape(B, Hq, Hkv, N, total_tokens, d, cu_seqlens, s);
+    if (st != FA_OK) return st;
+    if (o_dtype != FA_BF16 && o_dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+    if (s.T == 0 || B == 0) return FA_OK;
+    if (!o || !dout || !D || !workspace) return FA_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(dout) || !aligned4(D) || !aligned16(workspace))
+        return FA_ERR_INVALID_ARG;
+    const BwdWs lay = bwd_ws_layout(B, Hq, Hkv, s.T, d);
+    if (workspace_bytes < lay.bytes) return FA_ERR_INVALID_ARG;
+    const int nsm = sm_count();
+    if (nsm <= 0) return FA_ERR_CUDA;
+    cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+    const int order = !causal ? kOrderSeqDesc : (deterministic ? kOrderLevelDesc : kOrderWorkDesc);
+    char* ws = static_cast<char*>(workspace);
+    cudaError_t e = launch_sched(cu_seqlens, B, N, Hq, kTile, order, lay.max_units, workspace,
+                                 lay.units, lay.tile_off, true, strm);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    e = launch_bwd_preprocess(o, o_dtype == FA_FP32, dout, D,
+                              reinterpret_cast<float*>(ws + lay.dq_acc),
+                              reinterpret_cast<int*>(ws + lay.sems), lay.max_qtiles * Hq, s.T, Hq,
+                              d, nsm, strm);
+    return cuda_status(e);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout, const float* lse,
+                 const float* D, void* dq, void* dk, void* dv, fa_dtype grad_dtype,
+                 void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N,
+                 int total_tokens, int d, float scale, int causal, const int* cu_seqlens,
+                 int deterministic, fa_stream_t stream) {
+    Shape s;
+    fa_status st = check_shape(B, Hq, Hkv, N, total_tokens, d, cu_seqlens, s);
+    if (st != FA_OK) return st;
+    if (grad_dtype != FA_BF16 && grad_dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_UNSUPPORTED;
+    if (s.T == 0 || B == 0) return FA_OK;
+    if (!q || !k || !v || !dout || !lse || !D || !dq || !dk || !dv || !workspace)
+        return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv) || !aligned4(lse) || !aligned4(D) || !aligned16(workspace))
+        return FA_ERR_INVALID_ARG;
+    const BwdWs lay = bwd_ws_layout(B, Hq, Hkv, s.T, d);
+    if (workspace_bytes < lay.bytes) return FA_ERR_INVALID_ARG;
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!make_map(&p.tm_q, q, s.T, Hq, d) || !make_map(&p.tm_k, k, s.T, Hkv, d) ||
+        !make_map(&p.tm_v, v, s.T, Hkv, d) || !make_map(&p.tm_do, dout, s.T, Hq, d))
+        return FA_ERR_CUDA;
+    p.lse = lse;
+    p.D = D;
+    p.dk = dk;
+    p.dv = dv;
+    p.cu_seqlens = cu_seqlens;
+    p.workspace = workspace;
+    p.units_off = lay.units;
+    p.tile_off_off = lay.tile_off;
+    p.sems_off = lay.sems;
+    p.dq_acc_off = lay.dq_acc;
+    p.dk_acc_off = lay.dk_acc;
+    p.dv_acc_off = lay.dv_acc;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.T = s.T; p.d = d;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.causal = causal ? 1 : 0;
+    p.deterministic = deterministic ? 1 : 0;
+    p.grad_fp32 = grad_dtype == FA_FP32;
+    const int nsm = sm_count();
+    if (nsm <= 0) return FA_ERR_CUDA;
+    cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_bwd(p, nsm, strm);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    char* ws = static_cast<char*>(workspace);
+    const bool gqa = Hq != Hkv;
+    e = launch_bwd_postprocess(reinterpret_cast<const float*>(ws + lay.dq_acc), dq,
+                               gqa ? reinterpret_cast<const float*>(ws + lay.dk_acc) : nullptr,
+                               gqa ? reinterpret_cast<const float*>(ws + lay.dv_acc) : nullptr,
+                               dk, dv, s.T, Hq, Hkv, d, scale, p.grad_fp32, nsm, strm);
+    return cuda_status(e);
+}
+
+fa_status fa_check_device_status(const void* workspace, fa_stream_t stream) {
+    if (!workspace) return FA_ERR_INVALID_ARG;
+    cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(strm) != cudaSuccess) return FA_ERR_CUDA;
+    int err = 0;
+    if (cudaMemcpyAsync(&err, workspace, sizeof(int), cudaMemcpyDeviceToHost, strm) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(strm) != cudaSuccess) return FA_ERR_CUDA;
+    if (err & kErrTimeout) return FA_ERR_TIMEOUT;
+    if (err & kErrSchedule) return FA_ERR_INVALID_ARG;
+    if (err) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,778 @@
+// bwd.cu -- tiled exact-attention backward for sm_103a: preprocess (D and
+// workspace reset), the main backward kernel, and the postprocess (dQ
+// conversion, GQA dK/dV reduction).
+//
+// Method: the backward is five products ("FlashAttention-4反向传播优化"
+// section 1.1): S = QK^T recomputed, P = exp(S - LSE) from the stored
+// logsumexp, dV += P^T dO, dP = dO V^T, dS = P * (dP - D), dK += dS^T Q,
+// dQ += dS K.  Work is parallel over key/value tiles ("FlashAttention-2-
+// ICLR24" 核心方法 2): a unit owns one key/value tile of one (sequence, query
+// head), keeps K_j, V_j and the dK_j, dV_j accumulators on chip, and walks the
+// query tiles; dQ is a sum over key/value tiles and is merged in global
+// memory, either with fp32 atomics or -- deterministic mode, section 3.2 of
+// the same page -- in a fixed order enforced by one semaphore per dQ tile.
+//
+// Walk order (section 3.3.1): unit j visits query tiles i = j, j+1, ...
+// (wrapping around for non-causal attention), so the contribution of unit j
+// to dQ tile i is the ((i - j) mod n)-th one, contributions to a tile arrive
+// in descending j, and under the causal mask no unit waits on its first dQ
+// write.  The scheduler launches units with descending j in deterministic
+// mode, and heaviest-first otherwise.
+//
+// Roles (384 threads):
+//   warp 0       producer: K_j, V_j once per unit, then Q_i, dO_i (TMA) and
+//                LSE_i, D_i (plain loads) through a 2-stage ring
+//   warp 1       MMA issuer (tcgen05, one thread)
+//   warp 2       TMEM allocation
+//   warps 4..7   compute: one thread per key row; P^T = exp2(S^T*c - LSE2),
+//                written bf16 to TMEM (A operand of dV); dS^T = P^T (dP^T - D)
+//                written bf16 to shared memory (A operand of dK, K-major, and
+//                of dQ, read as MN-major)
+//   warps 8..11  dQ drain (one thread per query row; atomic or ordered adds)
+//                and the dK/dV epilogue (one thread per key row)
+// TMEM: S^T [0,128) with P^T over [0,64); dP^T [128,256); dK [256,256+d);
+// dV [256+d, 256+2d); dQ reuses dP^T's columns for d = 128 and has its own
+// columns [384,448) for d = 64.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBwdThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kTileBytes = kTile * D * 2;
+    static constexpr int kBoxes = D / 64;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 256 + D;
+    static constexpr uint32_t kColDQ = D == 128 ? 128 : 384;
+    static constexpr bool kDqAliasesDp = D == 128;
+};
+
+template <int D>
+struct BwdSmem {
+    alignas(1024) uint8_t k[BwdCfg<D>::kTileBytes];
+    alignas(1024) uint8_t v[BwdCfg<D>::kTileBytes];
+    alignas(1024) uint8_t q[2][BwdCfg<D>::kTileBytes];
+    alignas(1024) uint8_t dout[2][BwdCfg<D>::kTileBytes];
+    alignas(1024) uint8_t ds[kTile * kTile * 2];  // dS^T: 128 key rows x 128 query cols
+    float lse2[2][kTile];                          // LSE * log2(e) of the stage's query rows
+    float dd[2][kTile];                            // D of the stage's query rows
+    alignas(8) uint64_t sched_full[2], sched_empty[2];
+    uint64_t kv_full, kv_empty;
+    uint64_t qdo_full[2], qdo_empty[2];
+    uint64_t s_full, dp_full, p_ready, ds_ready, s_free, ds_free, dq_full, dq_free;
+    uint64_t dkv_full, dkv_free, drain;
+    int2 sched[2];
+    uint32_t tmem_base;
+    int abort_flag;
+    int zero;
+};
+static_assert(sizeof(BwdSmem<128>) <= 232448, "backward shared memory exceeds 227 KB");
+
+struct BUnit {
+    int b, j, h, g, t0, L, nt, ni;
+};
+
+__device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
+    BUnit x;
+    x.b = u.x;
+    x.j = unit_tile(u.y);
+    x.h = unit_head(u.y);
+    x.g = (int)(((long long)x.h * p.Hkv) / p.Hq);
+    seq_bounds(p.cu_seqlens, p.N, x.b, x.t0, x.L);
+    x.nt = cdiv(x.L, kTile);
+    x.ni = p.causal ? x.nt - x.j : x.nt;
+    return x;
+}
+
+// Query tile visited at step s of unit x.
+__device__ __forceinline__ int walk_tile(const BUnit& x, int s) {
+    int i = x.j + s;
+    return i >= x.nt ? i - x.nt : i;
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* flag, WsHeader* hdr, int code) {
+    *flag = 1;
+    atomicOr(&hdr->error, code);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* flag,
+                                              WsHeader* hdr) {
+    if (mbar_wait(bar, parity, flag)) return true;
+    raise_abort(flag, hdr, kErrTimeout);
+    return false;
+}
+
+// Whole-warp wait: every lane leaves with the same answer.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* flag,
+                                          WsHeader* hdr) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar, parity, flag, hdr));
+}
+
+// Wait shared by the four warps of the dQ/epilogue warpgroup: they meet on
+// named barrier 1 (deterministic mode), so all 128 threads must take the same
+// branch after every wait.
+__device__ __forceinline__ bool wg_wait(uint32_t bar, uint32_t parity, volatile int* flag,
+                                        WsHeader* hdr) {
+    return named_bar_and(1, 128, warp_wait(bar, parity, flag, hdr));
+}
+
+// Whole-warp wait done by lane 0 only (the producer warp).
+__device__ __forceinline__ bool lane0_wait(uint32_t bar, uint32_t parity, volatile int* flag,
+                                           WsHeader* hdr) {
+    int ok = 1;
+    if (lane_id() == 0) ok = wait_or_abort(bar, parity, flag, hdr) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until *sem == target (or some CTA already recorded an error).
+__device__ bool sem_wait(const int* sem, int target, const WsHeader* hdr) {
+    if (ld_acquire_gpu(sem) == target) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 16; ++i) {
+            __nanosleep(64);
+            if (ld_acquire_gpu(sem) == target) return true;
+        }
+        if (*reinterpret_cast<const volatile int*>(&hdr->error)) return false;
+        if (globaltimer() - t0 > kSpinLimitNs) return false;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+    using Cfg = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(p.workspace);
+    if (smem_u32(smem_raw) & 1023u) {  // layout relies on a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicOr(&hdr->error, kErrSmemAlign);
+        return;
+    }
+    BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
+    const char* ws = static_cast<const char*>(p.workspace);
+    const int2* units = reinterpret_cast<const int2*>(ws + p.units_off);
+    const int* tile_off = reinterpret_cast<const int*>(ws + p.tile_off_off);
+    int* sems = reinterpret_cast<int*>(static_cast<char*>(p.workspace) + p.sems_off);
+    float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + p.dq_acc_off);
+    float* dk_acc = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + p.dk_acc_off);
+    float* dv_acc = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + p.dv_acc_off);
+    const int warp = warp_id(), lane = lane_id();
+    volatile int* abort_flag = &sm.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&sm.sched_full[i]), 1);
+            mbar_init(smem_u32(&sm.sched_empty[i]), 1 + 8);
+            mbar_init(smem_u32(&sm.qdo_full[i]), 1 + 32);
+            mbar_init(smem_u32(&sm.qdo_empty[i]), 1);
+        }
+        mbar_init(smem_u32(&sm.kv_full), 1);
+        mbar_init(smem_u32(&sm.kv_empty), 1);
+        mbar_init(smem_u32(&sm.s_full), 1);
+        mbar_init(smem_u32(&sm.dp_full), 1);
+        mbar_init(smem_u32(&sm.p_ready), 4);
+        mbar_init(smem_u32(&sm.ds_ready), 4);
+        mbar_init(smem_u32(&sm.s_free), 1);
+        mbar_init(smem_u32(&sm.ds_free), 1);
+        mbar_init(smem_u32(&sm.dq_full), 1);
+        mbar_init(smem_u32(&sm.dq_free), 4);
+        mbar_init(smem_u32(&sm.dkv_full), 1);
+        mbar_init(smem_u32(&sm.dkv_free), 4);
+        mbar_init(smem_u32(&sm.drain), 1);
+        sm.abort_flag = 0;
+        sm.zero = 0;
+        fence_barrier_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(&sm.tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const int n_units = hdr->n_units;
+    const int n_qtiles = hdr->n_qtiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            tma_prefetch_desc(&p.tm_do);
+        }
+        int sched_it = 0, unit_it = 0, qit = 0;
+        bool ok = true;
+        while (ok) {
+            const int slot = sched_it & 1;
+            if (!(ok = lane0_wait(smem_u32(&sm.sched_empty[slot]), ((sched_it >> 1) & 1) ^ 1,
+                                  abort_flag, hdr)))
+                break;
+            int2 unit = make_int2(-1, 0);
+            if (lane == 0) {
+                const int u = atomicAdd(&hdr->counter, 1);
+                if (u < n_units) unit = units[u];
+                sm.sched[slot] = unit;
+                mbar_arrive(smem_u32(&sm.sched_full[slot]));
+            }
+            unit.x = __shfl_sync(0xffffffffu, unit.x, 0);
+            unit.y = __shfl_sync(0xffffffffu, unit.y, 0);
+            ++sched_it;
+            if (unit.x < 0) break;
+            const BUnit x = decode_bunit(unit, p);
+            if (!(ok = lane0_wait(smem_u32(&sm.kv_empty), (unit_it & 1) ^ 1, abort_flag, hdr)))
+                break;
+            if (lane == 0) {
+                const uint32_t bar = smem_u32(&sm.kv_full);
+                mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
+                for (int c = 0; c < Cfg::kBoxes; ++c) {
+                    tma_load_3d(smem_u32(sm.k) + c * 16384, &p.tm_k, bar, c * 64, x.g,
+                                x.t0 + x.j * kTile);
+                    tma_load_3d(smem_u32(sm.v) + c * 16384, &p.tm_v, bar, c * 64, x.g,
+                                x.t0 + x.j * kTile);
+                }
+            }
+            ++unit_it;
+            for (int s = 0; s < x.ni && ok; ++s) {
+                const int i = walk_tile(x, s);
+                const int st = qit & 1;
+                if (!(ok = lane0_wait(smem_u32(&sm.qdo_empty[st]), ((qit >> 1) & 1) ^ 1,
+                                      abort_flag, hdr)))
+                    break;
+                const uint32_t bar = smem_u32(&sm.qdo_full[st]);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
+                    for (int c = 0; c < Cfg::kBoxes; ++c) {
+                        tma_load_3d(smem_u32(sm.q[st]) + c * 16384, &p.tm_q, bar, c * 64, x.h,
+                                    x.t0 + i * kTile);
+                        tma_load_3d(smem_u32(sm.dout[st]) + c * 16384, &p.tm_do, bar, c * 64, x.h,
+                                    x.t0 + i * kTile);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = lane * 4 + e;
+                    const int r = i * kTile + rr;
+                    float l2 = 0.f, dv = 0.f;
+                    if (r < x.L) {
+                        const size_t at = (size_t)x.h * p.T + (size_t)(x.t0 + r);
+                        l2 = p.lse[at] * kLog2e;
+                        dv = p.D[at];
+                    }
+                    sm.lse2[st][rr] = l2;
+                    sm.dd[st][rr] = dv;
+                }
+                mbar_arrive(bar);
+                ++qit;
+            }
+        }
+        if (lane == 0) {
+            const volatile int* z = &sm.zero;
+            for (int e = 0; e < 2 && e < qit; ++e) {
+                const int it = qit - 1 - e;
+                mbar_wait(smem_u32(&sm.qdo_full[it & 1]), (it >> 1) & 1, z);
+            }
+            if (unit_it > 0) mbar_wait(smem_u32(&sm.kv_full), (unit_it - 1) & 1, z);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idKV = make_idesc_bf16(128, D, false, true);
+            constexpr uint32_t idDQ = make_idesc_bf16(128, D, true, true);
+            int sched_it = 0, unit_it = 0, qit = 0, cnt = 0;
+            bool ok = true;
+            const uint32_t kaddr = smem_u32(sm.k), vaddr = smem_u32(sm.v), dsaddr = smem_u32(sm.ds);
+            while (ok) {
+                const int slot = sched_it & 1;
+                if (!(ok = wait_or_abort(smem_u32(&sm.sched_full[slot]), (sched_it >> 1) & 1,
+                                         abort_flag, hdr)))
+                    break;
+                const int2 unit = sm.sched[slot];
+                mbar_arrive(smem_u32(&sm.sched_empty[slot]));
+                ++sched_it;
+                if (unit.x < 0) break;
+                const BUnit x = decode_bunit(unit, p);
+                if (!(ok = wait_or_abort(smem_u32(&sm.kv_full), unit_it & 1, abort_flag, hdr))) break;
+                for (int s = 0; s < x.ni; ++s) {
+                    const int st = qit & 1;
+                    if (!(ok = wait_or_abort(smem_u32(&sm.qdo_full[st]), (qit >> 1) & 1, abort_flag,
+                                             hdr)))
+                        break;
+                    const uint32_t qaddr = smem_u32(sm.q[st]), doaddr = smem_u32(sm.dout[st]);
+                    // S^T = K_j Q_i^T  (the S region is free once dV of the previous step ran)
+                    if (cnt > 0 && !(ok = wait_or_abort(smem_u32(&sm.s_free), (cnt - 1) & 1,
+                                                        abort_flag, hdr)))
+                        break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tmem + Cfg::kColS, make_sdesc(kaddr + off, 16, 1024),
+                               make_sdesc(qaddr + off, 16, 1024), idS, kk > 0);
+                    }
+                    mma_commit(smem_u32(&sm.s_full));
+                    // dP^T = V_j dO_i^T  (for d = 128 the dQ drain of the previous step shares columns)
+                    if (Cfg::kDqAliasesDp && cnt > 0 &&
+                        !(ok = wait_or_abort(smem_u32(&sm.dq_free), (cnt - 1) & 1, abort_flag, hdr)))
+                        break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tmem + Cfg::kColDP, make_sdesc(vaddr + off, 16, 1024),
+                               make_sdesc(doaddr + off, 16, 1024), idS, kk > 0);
+                    }
+                    mma_commit(smem_u32(&sm.dp_full));
+                    // dV_j += P^T dO_i  (A = P^T from TMEM)
+                    if (!(ok = wait_or_abort(smem_u32(&sm.p_ready), cnt & 1, abort_flag, hdr))) break;
+                    if (s == 0 && unit_it > 0 &&
+                        !(ok = wait_or_abort(smem_u32(&sm.dkv_free), (unit_it - 1) & 1, abort_flag,
+                                             hdr)))
+                        break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + kk * 8,
+                               make_sdesc(doaddr + kk * 2048, 16384, 1024), idKV,
+                               (s > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&sm.s_free));
+                    // dK_j += dS^T Q_i ; dQ_i = dS K_j  (A = dS^T in shared memory)
+                    if (!(ok = wait_or_abort(smem_u32(&sm.ds_ready), cnt & 1, abort_flag, hdr))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tmem + Cfg::kColDK, make_sdesc(dsaddr + off, 16, 1024),
+                               make_sdesc(qaddr + kk * 2048, 16384, 1024), idKV,
+                               (s > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (!Cfg::kDqAliasesDp && cnt > 0 &&
+                        !(ok = wait_or_abort(smem_u32(&sm.dq_free), (cnt - 1) & 1, abort_flag, hdr)))
+                        break;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ss(tmem + Cfg::kColDQ, make_sdesc(dsaddr + kk * 2048, 16384, 1024),
+                               make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ, kk > 0);
+                    mma_commit(smem_u32(&sm.dq_full));
+                    mma_commit(smem_u32(&sm.ds_free));
+                    mma_commit(smem_u32(&sm.qdo_empty[st]));
+                    ++cnt;
+                    ++qit;
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&sm.dkv_full));
+                mma_commit(smem_u32(&sm.kv_empty));
+                ++unit_it;
+            }
+            mma_commit(smem_u32(&sm.drain));
+            mbar_wait(smem_u32(&sm.drain), 0, &sm.zero);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ compute: P^T and dS^T
+        const int q4 = warp & 3;
+        const int rk = q4 * 32 + lane;                    // key row within the tile (TMEM lane)
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const uint32_t s_addr = tmem + lane_off + Cfg::kColS;
+        const uint32_t dp_addr = tmem + lane_off + Cfg::kColDP;
+        uint8_t* ds_row = sm.ds + rk * 128;
+        const int sw = rk & 7;
+        int sched_it = 0, qit = 0, cnt = 0;
+        bool ok = true;
+        while (ok) {
+            const int slot = sched_it & 1;
+            if (!(ok = warp_wait(smem_u32(&sm.sched_full[slot]), (sched_it >> 1) & 1, abort_flag,
+                                 hdr)))
+                break;
+            const int2 unit = sm.sched[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
+            ++sched_it;
+            if (unit.x < 0) break;
+            const BUnit x = decode_bunit(unit, p);
+            const int c = x.j * kTile + rk;  // key position within the sequence
+            for (int s = 0; s < x.ni; ++s) {
+                const int i = walk_tile(x, s);
+                const int st = qit & 1;
+                // visible query columns of this key row: [lo, hi)
+                const int lo = p.causal ? max(0, c - i * kTile) : 0;
+                const int hi = c < x.L ? min(kTile, x.L - i * kTile) : 0;
+                if (!(ok = warp_wait(smem_u32(&sm.qdo_full[st]), (qit >> 1) & 1, abort_flag, hdr)))
+                    break;
+                if (!(ok = warp_wait(smem_u32(&sm.s_full), cnt & 1, abort_flag, hdr))) break;
+                tc_fence_after();
+                const float* l2 = sm.lse2[st];
+                uint32_t pk[64];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sv[32];
+                    tmem_ld32(s_addr + cc * 32, sv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int x0 = cc * 32 + 2 * e, x1 = x0 + 1;
+                        const float p0 = (x0 >= lo && x0 < hi)
+                                             ? ex2_approx(fmaf(__uint_as_float(sv[2 * e]),
+                                                               p.scale_log2, -l2[x0]))
+                                             : 0.f;
+                        const float p1 = (x1 >= lo && x1 < hi)
+                                             ? ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]),
+                                                               p.scale_log2, -l2[x1]))
+                                             : 0.f;
+                        pk[cc * 16 + e] = pack_bf16x2(p0, p1);
+                    }
+                    uint32_t chunk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) chunk[e] = pk[cc * 16 + e];
+                    tmem_st16(s_addr + cc * 16, chunk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sm.p_ready));
+                // dS^T = P^T * (dP^T - D), bf16, swizzled rows of the dS^T tile
+                if (!(ok = warp_wait(smem_u32(&sm.dp_full), cnt & 1, abort_flag, hdr))) break;
+                if (cnt > 0 &&
+                    !(ok = warp_wait(smem_u32(&sm.ds_free), (cnt - 1) & 1, abort_flag, hdr)))
+                    break;
+                tc_fence_after();
+                const float* dd = sm.dd[st];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t dv[32];
+                    tmem_ld32(dp_addr + cc * 32, dv);
+                    tmem_ld_wait();
+                    uint32_t out[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int x0 = cc * 32 + 2 * e;
+                        __nv_bfloat162 pp = *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + e]);
+                        const float2 pf = __bfloat1622float2(pp);
+                        const float d0 = pf.x * (__uint_as_float(dv[2 * e]) - dd[x0]);
+                        const float d1 = pf.y * (__uint_as_float(dv[2 * e + 1]) - dd[x0 + 1]);
+                        out[e] = pack_bf16x2(d0, d1);
+                    }
+                    // 32 query columns = 4 chunks of 16 bytes in block (cc >> 1)
+                    uint8_t* blk = ds_row + (cc >> 1) * 16384;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int ch = (cc & 1) * 4 + e;
+                        *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
+                            make_uint4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sm.ds_ready));
+                ++cnt;
+                ++qit;
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+        const int q4 = warp & 3;
+        const int rr = q4 * 32 + lane;  // row within the tile (TMEM lane)
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const bool leader = (warp == 8 && lane == 0);
+        int sched_it = 0, unit_it = 0, cnt = 0;
+        bool ok = true;
+        while (ok) {
+            const int slot = sched_it & 1;
+            if (!(ok = wg_wait(smem_u32(&sm.sched_full[slot]), (sched_it >> 1) & 1, abort_flag,
+                               hdr)))
+                break;
+            const int2 unit = sm.sched[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
+            ++sched_it;
+            if (unit.x < 0) break;
+            const BUnit x = decode_bunit(unit, p);
+            for (int s = 0; s < x.ni; ++s) {
+                const int i = walk_tile(x, s);
+                if (!(ok = wg_wait(smem_u32(&sm.dq_full), cnt & 1, abort_flag, hdr))) break;
+                tc_fence_after();
+                int* sem = nullptr;
+                bool sem_ok = true;
+                if (p.deterministic) {
+                    sem = sems + (size_t)x.h * n_qtiles + tile_off[x.b] + i;
+                    if (leader) {
+                        int target = i - x.j;
+                        if (target < 0) target += x.nt;
+                        sem_ok = sem_wait(sem, target, hdr);
+                        if (!sem_ok) raise_abort(abort_flag, hdr, kErrTimeout);
+                    }
+                    sem_ok = named_bar_and(1, 128, sem_ok);
+                }
+                const int qr = i * kTile + rr;
+                const bool valid = qr < x.L && sem_ok;
+                float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v);
+                    tmem_ld_wait();
+                    if (valid) {
+                        float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            atomicAdd(d4 + e, make_float4(__uint_as_float(v[4 * e]),
+                                                          __uint_as_float(v[4 * e + 1]),
+                                                          __uint_as_float(v[4 * e + 2]),
+                                                          __uint_as_float(v[4 * e + 3])));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
+                if (p.deterministic) {
+                    __threadfence();
+                    named_bar_sync(1, 128);
+                    if (leader && sem_ok) red_release_gpu_add(sem, 1);
+                }
+                ++cnt;
+                if (!sem_ok) { ok = false; break; }
+            }
+            if (!ok) break;
+            // dK_j (times scale) and dV_j for this query head
+            if (!(ok = wg_wait(smem_u32(&sm.dkv_full), unit_it & 1, abort_flag, hdr))) break;
+            tc_fence_after();
+            const int kr = x.j * kTile + rr;
+            const bool valid = kr < x.L;
+            const size_t tok = (size_t)x.t0 + (size_t)kr;
+            const bool gqa = p.Hq != p.Hkv;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which == 0 ? Cfg::kColDK : Cfg::kColDV;
+                const float mul = which == 0 ? p.scale : 1.f;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + col + cc * 32, v);
+                    tmem_ld_wait();
+                    if (!valid) continue;
+                    if (gqa) {
+                        float* acc = (which == 0 ? dk_acc : dv_acc) + (tok * p.Hq + x.h) * D + cc * 32;
+                        float4* d4 = reinterpret_cast<float4*>(acc);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul,
+                                                __uint_as_float(v[4 * e + 1]) * mul,
+                                                __uint_as_float(v[4 * e + 2]) * mul,
+                                                __uint_as_float(v[4 * e + 3]) * mul);
+                    } else if (p.grad_fp32) {
+                        float* out = static_cast<float*>(which == 0 ? p.dk : p.dv) +
+                                     (tok * p.Hkv + x.g) * D + cc * 32;
+                        float4* d4 = reinterpret_cast<float4*>(out);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul,
+                                                __uint_as_float(v[4 * e + 1]) * mul,
+                                                __uint_as_float(v[4 * e + 2]) * mul,
+                                                __uint_as_float(v[4 * e + 3]) * mul);
+                    } else {
+                        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(which == 0 ? p.dk : p.dv) +
+                                             (tok * p.Hkv + x.g) * D + cc * 32;
+                        uint4* d4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            d4[e] = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[8 * e]) * mul,
+                                            __uint_as_float(v[8 * e + 1]) * mul),
+                                pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul,
+                                            __uint_as_float(v[8 * e + 3]) * mul),
+                                pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul,
+                                            __uint_as_float(v[8 * e + 5]) * mul),
+                                pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul,
+                                            __uint_as_float(v[8 * e + 7]) * mul));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.dkv_free));
+            ++unit_it;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// D = rowsum(dO * O) per (token, head); zero the dQ accumulator row and the semaphores.
+template <int D, bool O_FP32>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_kernel(const void* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                          float* __restrict__ Dout, float* __restrict__ dq_acc,
+                          int* __restrict__ sems, long long n_sems, int T, int Hq) {
+    const long long rows = (long long)T * Hq;
+    const long long warp_g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr int E = D / 32;  // elements per lane
+    for (long long r = warp_g; r < rows; r += nwarps) {
+        const long long t = r / Hq, h = r % Hq;
+        const size_t base = (size_t)r * D + lane * E;
+        float acc = 0.f;
+        float ov[E], dv[E];
+        if (O_FP32) {
+            const float* op = static_cast<const float*>(o) + base;
+#pragma unroll
+            for (int e = 0; e < E; ++e) ov[e] = op[e];
+        } else {
+            const __nv_bfloat16* op = static_cast<const __nv_bfloat16*>(o) + base;
+#pragma unroll
+            for (int e = 0; e < E; ++e) ov[e] = __bfloat162float(op[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) dv[e] = __bfloat162float(dout[base + e]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc = fmaf(ov[e], dv[e], acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) Dout[(size_t)h * T + (size_t)t] = acc;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dq_acc[base + e] = 0.f;
+    }
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (long long s = tid; s < n_sems; s += (long long)gridDim.x * blockDim.x) sems[s] = 0;
+}
+
+// dq = scale * dq_acc; for GQA, dk/dv[t,g] = sum over the group's query heads h
+// (in increasing h) of the per-head partials.  One flat index space of float4
+// groups: [0, nq) dq, [nq, nq+nkv) dk, [nq+nkv, nq+2nkv) dv.
+template <int D, bool F32>
+__global__ void __launch_bounds__(256)
+    bwd_postprocess_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq,
+                           const float* __restrict__ dk_acc, const float* __restrict__ dv_acc,
+                           void* __restrict__ dk, void* __restrict__ dv, int T, int Hq, int Hkv,
+                           float scale) {
+    constexpr int V = D / 4;  // float4 groups per row
+    const long long nq = (long long)T * Hq * V;
+    const long long nkv = dk_acc ? (long long)T * Hkv * V : 0;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const int grp = Hq / Hkv;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nq + 2 * nkv;
+         e += stride) {
+        float4 r;
+        void* out;
+        long long oi;
+        if (e < nq) {
+            const float4 a = reinterpret_cast<const float4*>(dq_acc)[e];
+            r = make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale);
+            out = dq;
+            oi = e;
+        } else {
+            const bool is_v = e >= nq + nkv;
+            oi = e - nq - (is_v ? nkv : 0);
+            const long long row = oi / V;  // (t, g)
+            const int c4 = (int)(oi % V);
+            const long long t = row / Hkv;
+            const int g = (int)(row % Hkv);
+            const float4* src = reinterpret_cast<const float4*>(is_v ? dv_acc : dk_acc);
+            r = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int hh = 0; hh < grp; ++hh) {
+                const float4 a = src[(t * Hq + (long long)g * grp + hh) * V + c4];
+                r.x += a.x; r.y += a.y; r.z += a.z; r.w += a.w;
+            }
+            out = is_v ? dv : dk;
+        }
+        if (F32) {
+            reinterpret_cast<float4*>(out)[oi] = r;
+        } else {
+            reinterpret_cast<uint2*>(out)[oi] =
+                make_uint2(pack_bf16x2(r.x, r.y), pack_bf16x2(r.z, r.w));
+        }
+    }
+}
+
+int grid_for(long long work, int threads, int num_sms) {
+    long long g = (work + threads - 1) / threads;
+    const long long cap = (long long)num_sms * 8;
+    if (g > cap) g = cap;
+    return (int)(g < 1 ? 1 : g);
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const BwdParams& p, int num_sms, cudaStream_t stream) {
+    auto kern = fa_bwd_kernel<D>;
+    const size_t smem = sizeof(BwdSmem<D>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long bound = max_tiles(p.B, p.T, kTile) * p.Hq;
+    const int grid = (int)(bound < num_sms ? bound : num_sms);
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, kBwdThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, float* D,
+                                  float* dq_acc, int* sems, long long n_sems, int T, int Hq,
+                                  int d, int num_sms, cudaStream_t stream) {
+    const long long rows = (long long)T * Hq;
+    const int grid = grid_for(rows * 32 > n_sems ? rows * 32 : n_sems, 256, num_sms);
+    const __nv_bfloat16* dob = static_cast<const __nv_bfloat16*>(dout);
+#define FA_PRE(DD, FF) \
+    bwd_preprocess_kernel<DD, FF><<<grid, 256, 0, stream>>>(o, dob, D, dq_acc, sems, n_sems, T, Hq)
+    if (d == 128) {
+        if (o_fp32) FA_PRE(128, true); else FA_PRE(128, false);
+    } else {
+        if (o_fp32) FA_PRE(64, true); else FA_PRE(64, false);
+    }
+#undef FA_PRE
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream) {
+    return p.d == 128 ? launch_bwd_t<128>(p, num_sms, stream) : launch_bwd_t<64>(p, num_sms, stream);
+}
+
+cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const float* dk_acc,
+                                   const float* dv_acc, void* dk, void* dv, int T, int Hq,
+                                   int Hkv, int d, float scale, int grad_fp32, int num_sms,
+                                   cudaStream_t stream) {
+    const long long work = (long long)T * (Hq + (dk_acc ? 2 * Hkv : 0)) * d / 4;
+    const int grid = grid_for(work, 256, num_sms);
+#define FA_POST(DD, FF)                                                                         \
+    bwd_postprocess_kernel<DD, FF><<<grid, 256, 0, stream>>>(dq_acc, dq, dk_acc, dv_acc, dk, dv, \
+                                                             T, Hq, Hkv, scale)
+    if (d == 128) {
+        if (grad_fp32) FA_POST(128, true); else FA_POST(128, false);
+    } else {
+        if (grad_fp32) FA_POST(64, true); else FA_POST(64, false);
+    }
+#undef FA_POST
+    return cudaGetLastError();
+}
+
+}  // namespace fa

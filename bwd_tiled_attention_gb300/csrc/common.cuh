@@ -1,0 +1,104 @@
+// common.cuh -- definitions shared by the host launchers and the kernels:
+// tile sizes, workspace layouts, the work-unit encoding written by the tile
+// scheduler, and per-sequence geometry.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace fa {
+
+constexpr int kTile = 128;          // rows of one query tile / key-value tile
+constexpr int kFwdBlockRows = 256;  // query rows of one forward work unit (two tiles)
+constexpr size_t kAlign = 256;      // alignment of every workspace segment
+
+// Device error word bits (workspace offset 0).
+constexpr int kErrTimeout = 1;      // a bounded wait gave up
+constexpr int kErrSmemAlign = 2;    // dynamic shared memory not 1024-byte aligned
+constexpr int kErrSchedule = 4;     // scheduler metadata inconsistent (a length > N)
+
+// Header of every workspace (first kAlign bytes).
+struct WsHeader {
+    int error;          // device error word (kErr* bits)
+    int counter;        // dynamic work-unit counter (zeroed by the scheduler kernel)
+    int n_units;        // number of valid entries in the unit list
+    int n_qtiles;       // query tiles over all sequences (backward)
+};
+
+// Unit-list entry: x = sequence index, y = (tile index << 16) | head index.
+__host__ __device__ inline int unit_tile(int y) { return (int)((unsigned)y >> 16); }
+__host__ __device__ inline int unit_head(int y) { return y & 0xFFFF; }
+__host__ __device__ inline int make_unit_y(int tile, int head) { return (tile << 16) | head; }
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Upper bound on tiles of `rows` rows over all sequences of a batch:
+// sum_b ceil(L_b / rows) <= ceil(T / rows) + B.
+__host__ __device__ inline long long max_tiles(int B, int T, int rows) {
+    return (long long)cdiv(T, rows) + (long long)B;
+}
+
+// Forward workspace: header | unit list (int2).
+struct FwdWs {
+    size_t units;   // offset of the unit list
+    size_t bytes;   // total
+    long long max_units;
+};
+
+__host__ __device__ inline FwdWs fwd_ws_layout(int B, int Hq, int T) {
+    FwdWs w;
+    w.max_units = max_tiles(B, T, kFwdBlockRows) * (long long)Hq;
+    w.units = kAlign;
+    w.bytes = align_up(w.units + (size_t)w.max_units * 8, kAlign);
+    return w;
+}
+
+// Backward workspace: header | unit list (int2) | per-sequence query-tile
+// offsets (int[B+1]) | semaphores (int[Hq * max_qtiles]) | dQ accumulator
+// fp32 [T,Hq,d] | (GQA only) dK and dV partials fp32 [T,Hq,d].
+struct BwdWs {
+    size_t units, tile_off, sems, dq_acc, dk_acc, dv_acc, bytes;
+    long long max_units, max_qtiles;
+};
+
+__host__ __device__ inline BwdWs bwd_ws_layout(int B, int Hq, int Hkv, int T, int d) {
+    BwdWs w;
+    w.max_qtiles = max_tiles(B, T, kTile);
+    w.max_units = w.max_qtiles * (long long)Hq;
+    w.units = kAlign;
+    w.tile_off = align_up(w.units + (size_t)w.max_units * 8, kAlign);
+    w.sems = align_up(w.tile_off + (size_t)(B + 1) * 4, kAlign);
+    w.dq_acc = align_up(w.sems + (size_t)w.max_qtiles * (size_t)Hq * 4, kAlign);
+    size_t acc = (size_t)T * (size_t)Hq * (size_t)d * 4;
+    w.dk_acc = align_up(w.dq_acc + acc, kAlign);
+    if (Hq != Hkv) {
+        w.dv_acc = align_up(w.dk_acc + acc, kAlign);
+        w.bytes = align_up(w.dv_acc + acc, kAlign);
+    } else {
+        w.dv_acc = w.dk_acc;
+        w.bytes = w.dk_acc;
+    }
+    return w;
+}
+
+// Sequence geometry: start token and length of sequence b.
+__device__ __forceinline__ void seq_bounds(const int* cu_seqlens, int N, int b, int& t0, int& L) {
+    if (cu_seqlens) {
+        t0 = cu_seqlens[b];
+        L = cu_seqlens[b + 1] - t0;
+    } else {
+        t0 = b * N;
+        L = N;
+    }
+}
+
+// Orders the scheduler can write.
+enum SchedOrder : int {
+    kOrderLevelDesc = 0,   // causal: tile index descending across sequences (heaviest
+                           // forward query blocks first; lightest backward KV tiles first)
+    kOrderWorkDesc = 1,    // causal backward, atomic mode: KV tiles by remaining work,
+                           // heaviest first (tile index ascending within a sequence)
+    kOrderSeqDesc = 2,     // non-causal: sequences longest first, tiles in order
+};
+
+}  // namespace fa

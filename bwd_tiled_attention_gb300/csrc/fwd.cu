@@ -1,0 +1,468 @@
+// fwd.cu -- tiled exact-attention forward for sm_103a.
+//
+// Method ("FlashAttention-2-ICLR24", 核心方法 1 and 2): each work unit is a
+// block of query rows of one (sequence, head); an inner loop walks the
+// key/value tiles, keeping a running row max m and row sum l, an unnormalised
+// output O~ that is rescaled when m grows, and one division by l at the end;
+// only LSE = m + log l is stored.  Key/value tiles entirely above the causal
+// diagonal are never visited; only tiles that straddle it (or the ragged end
+// of a sequence) are masked.
+//
+// Blackwell design ("FlashAttention-4 wird offiziell veröffentlicht", section
+// "Neue Hardwaremerkmale von Blackwell": single-thread tcgen05.mma accumulating
+// in tensor memory, A operand readable from tensor memory, warp specialisation):
+//   warp 0       TMA producer: both query tiles of a unit once, then a ring of
+//                key and value tiles (128-byte swizzled, one box per 64 columns)
+//   warp 1       MMA issuer: S_t = Q_t K^T into TMEM, then O_t += P_t V with P_t
+//                read from TMEM
+//   warp 2       TMEM allocation
+//   warps 4..7   softmax for query tile 0 (one thread per row)
+//   warps 8..11  softmax for query tile 1
+// A unit covers 256 query rows (two 128-row tiles) so each K/V tile loaded
+// feeds two MMAs, and the tensor core works on one tile while the softmax
+// warps of the other tile run.  TMEM: S_0 [0,128), S_1 [128,256), O_0
+// [256,256+d), O_1 [384,384+d); P_t is written as bf16 over the first 64
+// columns of S_t.
+//
+// Softmax uses exp2 with the scale folded in (s * scale * log2 e).  The O~
+// rescale is conditional: the reference max is only moved when the row max
+// grows by more than 8 (a factor 256 in P), which keeps P in range while
+// skipping most rescales; the result is exact because l and O~ always share
+// the same reference.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kFwdThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kStages = D == 128 ? 2 : 4;
+    static constexpr int kTileBytes = kTile * D * 2;  // one 128-row bf16 tile
+    static constexpr int kBoxes = D / 64;             // 64-column TMA boxes per tile
+};
+
+template <int D>
+struct FwdSmem {
+    alignas(1024) uint8_t q[2][FwdCfg<D>::kTileBytes];
+    alignas(1024) uint8_t k[FwdCfg<D>::kStages][FwdCfg<D>::kTileBytes];
+    alignas(1024) uint8_t v[FwdCfg<D>::kStages][FwdCfg<D>::kTileBytes];
+    alignas(8) uint64_t sched_full[2], sched_empty[2];
+    uint64_t q_full, q_empty;
+    uint64_t k_full[FwdCfg<D>::kStages], v_full[FwdCfg<D>::kStages], kv_empty[FwdCfg<D>::kStages];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+    uint64_t drain;
+    int2 sched[2];
+    uint32_t tmem_base;
+    int abort_flag;
+    int zero;
+};
+
+struct UnitGeom {
+    int b, m, h, g, t0, L, n[2], nkv;
+};
+
+__device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
+    UnitGeom x;
+    x.b = u.x;
+    x.m = unit_tile(u.y);
+    x.h = unit_head(u.y);
+    x.g = (int)(((long long)x.h * p.Hkv) / p.Hq);
+    seq_bounds(p.cu_seqlens, p.N, x.b, x.t0, x.L);
+    const int r0 = x.m * kFwdBlockRows;
+    for (int t = 0; t < 2; ++t) {
+        const int rs = r0 + t * kTile;  // first row of tile t
+        if (rs >= x.L) {
+            x.n[t] = 0;
+        } else if (p.causal) {
+            const int re = min(rs + kTile, x.L);  // one past last valid row
+            x.n[t] = cdiv(re, kTile);
+        } else {
+            x.n[t] = cdiv(x.L, kTile);
+        }
+    }
+    x.nkv = max(x.n[0], x.n[1]);
+    return x;
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* flag, WsHeader* hdr, int code) {
+    *flag = 1;
+    atomicOr(&hdr->error, code);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* flag,
+                                              WsHeader* hdr) {
+    if (mbar_wait(bar, parity, flag)) return true;
+    raise_abort(flag, hdr, kErrTimeout);
+    return false;
+}
+
+// Whole-warp wait: every lane leaves with the same answer.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* flag,
+                                          WsHeader* hdr) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar, parity, flag, hdr));
+}
+
+template <int D, bool OUT_FP32>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+    using Cfg = FwdCfg<D>;
+    constexpr int S = Cfg::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(p.workspace);
+    const int2* units =
+        reinterpret_cast<const int2*>(static_cast<const char*>(p.workspace) + p.units_off);
+    const int warp = warp_id(), lane = lane_id();
+    volatile int* abort_flag = &sm.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&sm.sched_full[i]), 1);
+            mbar_init(smem_u32(&sm.sched_empty[i]), 1 + 8);
+            mbar_init(smem_u32(&sm.s_full[i]), 1);
+            mbar_init(smem_u32(&sm.p_full[i]), 4);
+            mbar_init(smem_u32(&sm.o_done[i]), 1);
+            mbar_init(smem_u32(&sm.o_free[i]), 4);
+        }
+        mbar_init(smem_u32(&sm.q_full), 1);
+        mbar_init(smem_u32(&sm.q_empty), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&sm.k_full[s]), 1);
+            mbar_init(smem_u32(&sm.v_full[s]), 1);
+            mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&sm.drain), 1);
+        sm.abort_flag = 0;
+        sm.zero = 0;
+        fence_barrier_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(&sm.tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const int n_units = hdr->n_units;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            int sched_it = 0, kv_it = 0, unit_it = 0;
+            bool ok = true;
+            while (ok) {
+                const int slot = sched_it & 1;
+                if (!(ok = wait_or_abort(smem_u32(&sm.sched_empty[slot]),
+                                         ((sched_it >> 1) & 1) ^ 1, abort_flag, hdr)))
+                    break;
+                const int u = atomicAdd(&hdr->counter, 1);
+                const int2 unit = u < n_units ? units[u] : make_int2(-1, 0);
+                sm.sched[slot] = unit;
+                mbar_arrive(smem_u32(&sm.sched_full[slot]));
+                ++sched_it;
+                if (unit.x < 0) break;
+                const UnitGeom x = decode_unit(unit, p);
+                const int row0 = x.t0 + x.m * kFwdBlockRows;
+                if (!(ok = wait_or_abort(smem_u32(&sm.q_empty), (unit_it & 1) ^ 1, abort_flag, hdr)))
+                    break;
+                const uint32_t qbar = smem_u32(&sm.q_full);
+                mbar_arrive_expect_tx(qbar, (x.n[1] > 0 ? 2 : 1) * Cfg::kTileBytes);
+                for (int t = 0; t < 2; ++t) {
+                    if (x.n[t] == 0) continue;
+                    for (int c = 0; c < Cfg::kBoxes; ++c)
+                        tma_load_3d(smem_u32(sm.q[t]) + c * 16384, &p.tm_q, qbar, c * 64, x.h,
+                                    row0 + t * kTile);
+                }
+                ++unit_it;
+                for (int j = 0; j < x.nkv && ok; ++j) {
+                    const int st = kv_it % S;
+                    if (!(ok = wait_or_abort(smem_u32(&sm.kv_empty[st]), ((kv_it / S) & 1) ^ 1,
+                                             abort_flag, hdr)))
+                        break;
+                    const uint32_t kb = smem_u32(&sm.k_full[st]), vb = smem_u32(&sm.v_full[st]);
+                    mbar_arrive_expect_tx(kb, Cfg::kTileBytes);
+                    for (int c = 0; c < Cfg::kBoxes; ++c)
+                        tma_load_3d(smem_u32(sm.k[st]) + c * 16384, &p.tm_k, kb, c * 64, x.g,
+                                    x.t0 + j * kTile);
+                    mbar_arrive_expect_tx(vb, Cfg::kTileBytes);
+                    for (int c = 0; c < Cfg::kBoxes; ++c)
+                        tma_load_3d(smem_u32(sm.v[st]) + c * 16384, &p.tm_v, vb, c * 64, x.g,
+                                    x.t0 + j * kTile);
+                    ++kv_it;
+                }
+            }
+            // Never leave a TMA write in flight: wait (bounded) for the last
+            // phase armed on every load barrier.
+            const volatile int* z = &sm.zero;
+            for (int i = 0; i < S && i < kv_it; ++i) {
+                const int it = kv_it - 1 - i, st = it % S, par = (it / S) & 1;
+                mbar_wait(smem_u32(&sm.k_full[st]), par, z);
+                mbar_wait(smem_u32(&sm.v_full[st]), par, z);
+            }
+            if (unit_it > 0) mbar_wait(smem_u32(&sm.q_full), (unit_it - 1) & 1, z);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idPV = make_idesc_bf16(128, D, false, true);
+            int sched_it = 0, kv_it = 0, unit_it = 0;
+            int it[2] = {0, 0};   // PV MMAs issued per tile (= softmax iterations)
+            int ep[2] = {0, 0};   // units whose epilogue must finish before O_t is reused
+            bool ok = true;
+            while (ok) {
+                const int slot = sched_it & 1;
+                if (!(ok = wait_or_abort(smem_u32(&sm.sched_full[slot]), (sched_it >> 1) & 1,
+                                         abort_flag, hdr)))
+                    break;
+                const int2 unit = sm.sched[slot];
+                mbar_arrive(smem_u32(&sm.sched_empty[slot]));
+                ++sched_it;
+                if (unit.x < 0) break;
+                const UnitGeom x = decode_unit(unit, p);
+                if (!(ok = wait_or_abort(smem_u32(&sm.q_full), unit_it & 1, abort_flag, hdr)))
+                    break;
+                for (int j = 0; j < x.nkv && ok; ++j) {
+                    const int st = kv_it % S, par = (kv_it / S) & 1;
+                    if (!(ok = wait_or_abort(smem_u32(&sm.k_full[st]), par, abort_flag, hdr))) break;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= x.n[t]) continue;
+                        // S_t / P_t region is free once the previous O_t += P_t V is done
+                        if (it[t] > 0 &&
+                            !(ok = wait_or_abort(smem_u32(&sm.o_done[t]), (it[t] - 1) & 1,
+                                                 abort_flag, hdr)))
+                            break;
+                        tc_fence_after();
+                        const uint32_t qa = smem_u32(sm.q[t]), kb = smem_u32(sm.k[st]);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            mma_ss(tmem + t * 128, make_sdesc(qa + off, 16, 1024),
+                                   make_sdesc(kb + off, 16, 1024), idS, kk > 0);
+                        }
+                        mma_commit(smem_u32(&sm.s_full[t]));
+                    }
+                    if (!ok) break;
+                    // the unit's last S MMAs are issued: Q may be overwritten once they finish
+                    if (j == x.nkv - 1) mma_commit(smem_u32(&sm.q_empty));
+                    if (!(ok = wait_or_abort(smem_u32(&sm.v_full[st]), par, abort_flag, hdr))) break;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= x.n[t]) continue;
+                        if (!(ok = wait_or_abort(smem_u32(&sm.p_full[t]), it[t] & 1, abort_flag,
+                                                 hdr)))
+                            break;
+                        if (j == 0 && ep[t] > 0 &&
+                            !(ok = wait_or_abort(smem_u32(&sm.o_free[t]), (ep[t] - 1) & 1,
+                                                 abort_flag, hdr)))
+                            break;
+                        tc_fence_after();
+                        const uint32_t vb = smem_u32(sm.v[st]);
+                        const uint32_t o_col = 256 + t * 128, p_col = t * 128;
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ts(tmem + o_col, tmem + p_col + kk * 8,
+                                   make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(smem_u32(&sm.o_done[t]));
+                        ++it[t];
+                    }
+                    mma_commit(smem_u32(&sm.kv_empty[st]));
+                    ++kv_it;
+                }
+                if (!ok) break;
+                ++unit_it;
+                for (int t = 0; t < 2; ++t) ep[t] += x.n[t] > 0;
+            }
+            // all issued MMAs complete before TMEM is released
+            mma_commit(smem_u32(&sm.drain));
+            mbar_wait(smem_u32(&sm.drain), 0, &sm.zero);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = (warp - 4) >> 2;          // query tile of this warpgroup
+        const int q4 = warp & 3;                // TMEM lane quarter
+        const int row = q4 * 32 + lane;         // row within the tile
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const uint32_t s_addr = tmem + lane_off + t * 128;
+        const uint32_t o_addr = tmem + lane_off + 256 + t * 128;
+        int sched_it = 0, it = 0;
+        bool ok = true;
+        while (ok) {
+            const int slot = sched_it & 1;
+            if (!(ok = warp_wait(smem_u32(&sm.sched_full[slot]), (sched_it >> 1) & 1, abort_flag,
+                                 hdr)))
+                break;
+            const int2 unit = sm.sched[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
+            ++sched_it;
+            if (unit.x < 0) break;
+            const UnitGeom x = decode_unit(unit, p);
+            const int nt = x.n[t];
+            if (nt == 0) continue;
+            const int r = x.m * kFwdBlockRows + t * kTile + row;  // row within the sequence
+            const int limit = p.causal ? min(r + 1, x.L) : x.L;   // visible keys: col < limit
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < nt; ++j) {
+                if (!(ok = warp_wait(smem_u32(&sm.s_full[t]), it & 1, abort_flag, hdr))) break;
+                tc_fence_after();
+                float s[128];
+                {
+                    uint32_t raw[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld32(s_addr + c * 32, raw);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[i]);
+                    }
+                }
+                const int thr = limit - j * kTile;
+                if (thr < kTile) {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        if (i >= thr) s[i] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+                mx *= p.scale_log2;
+                float alpha = 1.f;
+                bool need = false;
+                if (j == 0) {
+                    m_ref = mx;
+                } else if (mx > m_ref + kRescaleThreshold) {
+                    need = true;
+                    alpha = ex2_approx(m_ref - mx);
+                    m_ref = mx;
+                    l *= alpha;
+                }
+                const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], p.scale_log2, neg));
+                        const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], p.scale_log2, neg));
+                        l += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(s_addr + c * 16, pk);
+                }
+                if (__any_sync(0xffffffffu, need)) {
+                    // O~ is stable here: S_t(j) was committed after O_t += P_t V of j-1.
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(o_addr + c * 32, ov);
+                        tmem_ld_wait();
+                        uint32_t lo[16], hi[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            lo[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                            hi[i] = __float_as_uint(__uint_as_float(ov[16 + i]) * alpha);
+                        }
+                        tmem_st16(o_addr + c * 32, lo);
+                        tmem_st16(o_addr + c * 32 + 16, hi);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[t]));
+                ++it;
+            }
+            if (!ok) break;
+            // epilogue: O = O~ / l, LSE = (m + log2 l) * ln 2
+            if (!(ok = warp_wait(smem_u32(&sm.o_done[t]), (it - 1) & 1, abort_flag, hdr))) break;
+            tc_fence_after();
+            const bool valid = r < x.L;
+            const float inv_l = 1.f / l;
+            const size_t tok = (size_t)x.t0 + (size_t)r;
+            if (valid) p.lse[(size_t)x.h * p.T + tok] = (m_ref + __log2f(l)) * 0.69314718055994531f;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(o_addr + c * 32, ov);
+                tmem_ld_wait();
+                if (valid) {
+                    const size_t base = (tok * p.Hq + x.h) * D + c * 32;
+                    if (OUT_FP32) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l,
+                                                 __uint_as_float(ov[4 * i + 1]) * inv_l,
+                                                 __uint_as_float(ov[4 * i + 2]) * inv_l,
+                                                 __uint_as_float(ov[4 * i + 3]) * inv_l);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + base);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(
+                                pack_bf16x2(__uint_as_float(ov[8 * i]) * inv_l,
+                                            __uint_as_float(ov[8 * i + 1]) * inv_l),
+                                pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv_l,
+                                            __uint_as_float(ov[8 * i + 3]) * inv_l),
+                                pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv_l,
+                                            __uint_as_float(ov[8 * i + 5]) * inv_l),
+                                pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv_l,
+                                            __uint_as_float(ov[8 * i + 7]) * inv_l));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.o_free[t]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool F32>
+cudaError_t launch_fwd_t(const FwdParams& p, int num_sms, cudaStream_t stream) {
+    auto kern = fa_fwd_kernel<D, F32>;
+    const size_t smem = sizeof(FwdSmem<D>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long bound = max_tiles(p.B, p.T, kFwdBlockRows) * p.Hq;
+    const int grid = (int)(bound < num_sms ? bound : num_sms);
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, kFwdThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams& p, int num_sms, cudaStream_t stream) {
+    if (p.d == 128)
+        return p.o_fp32 ? launch_fwd_t<128, true>(p, num_sms, stream)
+                        : launch_fwd_t<128, false>(p, num_sms, stream);
+    return p.o_fp32 ? launch_fwd_t<64, true>(p, num_sms, stream)
+                    : launch_fwd_t<64, false>(p, num_sms, stream);
+}
+
+}  // namespace fa

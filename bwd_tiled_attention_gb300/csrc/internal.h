@@ -1,0 +1,59 @@
+// internal.h -- host-side interfaces between the C ABI layer and the kernel
+// launchers (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+
+namespace fa {
+
+// Forward kernel arguments (device pointers, tensor maps built on the host).
+struct FwdParams {
+    CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [T, H, d], box {64, 1, 128}
+    void* o;
+    float* lse;
+    const int* cu_seqlens;         // null for dense
+    void* workspace;               // header + unit list
+    size_t units_off;
+    int B, Hq, Hkv, N, T, d;
+    float scale_log2;              // scale * log2(e)
+    int causal;
+    int o_fp32;
+};
+
+struct BwdParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    const float* lse;
+    const float* D;
+    void* dk;                      // final dK (MHA) -- bf16 or fp32
+    void* dv;
+    const int* cu_seqlens;
+    void* workspace;
+    size_t units_off, tile_off_off, sems_off, dq_acc_off, dk_acc_off, dv_acc_off;
+    int B, Hq, Hkv, N, T, d;
+    float scale;                   // softmax scale (dK and dQ factor)
+    float scale_log2;              // scale * log2(e)
+    int causal;
+    int deterministic;
+    int grad_fp32;
+};
+
+cudaError_t launch_sched(const int* cu_seqlens, int B, int N, int H, int rows, int order,
+                         long long max_units, void* workspace, size_t units_off,
+                         size_t tile_off_off, bool want_tile_off, cudaStream_t stream);
+
+cudaError_t launch_fwd(const FwdParams& p, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, float* D,
+                                  float* dq_acc, int* sems, long long n_sems, int T, int Hq,
+                                  int d, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const float* dk_acc,
+                                   const float* dv_acc, void* dk, void* dv, int T, int Hq,
+                                   int Hkv, int d, float scale, int grad_fp32, int num_sms,
+                                   cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,166 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) tiled exact-attention library.
+ *
+ * The library computes exact softmax attention and its gradients without ever
+ * forming the N x N score matrix.  Operation definitions follow
+ * "FlashAttention-2-ICLR24" (section 问题与动机: standard attention S = QK^T,
+ * P = softmax(S), O = PV, reproduced exactly by tiling plus online softmax;
+ * section 核心方法 1: deferred normalisation and a stored logsumexp only;
+ * section 核心方法 2: forward parallel over query-row blocks, backward parallel
+ * over key/value column blocks with dQ merged by atomic adds, causal blocks
+ * above the diagonal skipped; section 核心方法 4: MQA/GQA head mapping with
+ * dK/dV summed over the query heads sharing a key/value head), and
+ * "FlashAttention-4反向传播优化" (section 1.1: the backward is five products
+ * S, dP, dV, dK, dQ with P recomputed; section 3.2: deterministic mode
+ * serialises the global dQ reduction with semaphores; section 3.3: causal and
+ * variable-length tile scheduling).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers marked "device" are CUDA device pointers; the caller allocates
+ *   and owns every buffer, including the workspaces.  The library allocates
+ *   nothing and keeps no state besides cached device attributes.
+ * - Token-major packed layouts, head dim innermost and contiguous:
+ *     q, o, dout, dq : [T, Hq, d]      k, v, dk, dv : [T, Hkv, d]
+ *     lse, D         : [Hq, T] fp32
+ *   where T = total_tokens.  A dense batch (cu_seqlens == NULL) has T = B*N
+ *   and sequence b owns tokens [b*N, (b+1)*N).  A packed variable-length
+ *   batch passes cu_seqlens (device int32[B+1], cu_seqlens[0] = 0,
+ *   non-decreasing, cu_seqlens[B] = T), T as total_tokens, and N = an upper
+ *   bound on every sequence length (a longer sequence is reported as
+ *   FA_ERR_INVALID_ARG by fa_check_device_status and produces no output).
+ * - q, k, v, dout, dq, dk, dv and o must be 16-byte aligned (TMA).
+ * - Query head h uses key/value head floor(h * Hkv / Hq); Hq % Hkv == 0.
+ * - d must be 64 or 128.  Inputs are bf16.  scale multiplies QK^T (usually
+ *   1/sqrt(d)) and must be positive.  causal = 1 hides key j from query i
+ *   when j > i (positions within the sequence, top-left aligned; queries and
+ *   keys have equal length).
+ * - Every call is asynchronous on `stream` (NULL = the legacy default stream)
+ *   and never synchronises, except fa_check_device_status.  The return value
+ *   reports argument validation and launch errors only; it never aborts.
+ *   Errors found inside a kernel (a bounded wait that gave up) are recorded in
+ *   the workspace and reported by fa_check_device_status.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t, declared here without the CUDA headers. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, workspace too small */
+    FA_ERR_UNSUPPORTED = 2,  /* valid request outside what the kernels implement */
+    FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+    FA_ERR_TIMEOUT = 4       /* a bounded wait inside a kernel gave up (device-side) */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(fa_status s);
+
+/* Library build identifier (static string). */
+const char* fa_version(void);
+
+/*
+ * Workspace of fa_fwd, in bytes: a small header plus the ordered list of
+ * query-block work units that the on-device tile scheduler writes
+ * ("FlashAttention-4反向传播优化" section 3.3.2: a preprocessing kernel sorts
+ * sequences and writes the virtual-to-actual order the attention kernel walks).
+ * total_tokens = 0 means B*N.  Returns 0 for invalid sizes.
+ */
+size_t fa_fwd_workspace_size(int B, int Hq, int N, int total_tokens);
+
+/*
+ * Forward: O = softmax(scale * Q K^T + mask) V and LSE = natural-log
+ * logsumexp of the scaled, masked scores of each row ("FlashAttention-2-
+ * ICLR24", 核心方法 1: O is normalised once at the end; only LSE is stored).
+ *   q [T,Hq,d], k/v [T,Hkv,d]: device bf16, read only.
+ *   o [T,Hq,d]: device, written in o_dtype (FA_BF16 or FA_FP32).
+ *   lse [Hq,T]: device fp32, written.
+ *   workspace: device, >= fa_fwd_workspace_size(B,Hq,N,total_tokens) bytes,
+ *   16-byte aligned, contents scratch (rewritten each call).
+ * Returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED without launching anything
+ * when the arguments are wrong, FA_ERR_CUDA if a launch fails, FA_OK (and
+ * launches nothing) when there are no tokens.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype,
+                 float* lse, int B, int Hq, int Hkv, int N, int total_tokens, int d, float scale,
+                 int causal, const int* cu_seqlens, void* workspace, size_t workspace_bytes,
+                 fa_stream_t stream);
+
+/*
+ * Workspace of the backward pass (fa_bwd_preprocess + fa_bwd), in bytes: a
+ * header (device error word, work counter), the scheduler's ordered unit list
+ * and per-sequence tile offsets, one semaphore per (query head, query tile)
+ * for deterministic mode, the fp32 dQ accumulator [T,Hq,d], and -- when
+ * Hq != Hkv -- fp32 per-query-head dK/dV partials [T,Hq,d] each.
+ * Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int total_tokens, int d);
+
+/*
+ * Byte offset of the semaphore array inside the backward workspace (the
+ * device error word is the int at offset 0).  Semaphore (h, tile) is the int
+ * at index h * n_tiles + tile, where tiles are the 128-row query blocks
+ * numbered sequence after sequence and n_tiles is their total count.
+ */
+size_t fa_bwd_workspace_semaphore_offset(int B, int Hq, int Hkv, int N, int total_tokens, int d);
+
+/*
+ * Backward preprocess: D_i = sum_c dO_ic * O_ic for every query row (fp32),
+ * and reset of the backward workspace (zeroed dQ accumulator, semaphores,
+ * work counter and error word; the tile schedule is rebuilt).  The pages do
+ * not spell D out; it is the row term of dS = P * (dP - D) that follows from
+ * differentiating the softmax.
+ *   o [T,Hq,d]: device, o_dtype as written by fa_fwd.   dout [T,Hq,d]: device bf16.
+ *   D [Hq,T]: device fp32, written.
+ *   workspace: device, >= fa_bwd_workspace_size(...), 16-byte aligned.
+ * causal and deterministic select the unit order the scheduler writes; pass
+ * the same values to the fa_bwd call that follows.
+ */
+fa_status fa_bwd_preprocess(const void* o, fa_dtype o_dtype, const void* dout, float* D,
+                            void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                            int N, int total_tokens, int d, int causal,
+                            const int* cu_seqlens, int deterministic, fa_stream_t stream);
+
+/*
+ * Backward: dQ, dK, dV of L = sum(dO * O) for the forward above, recomputing P
+ * from LSE ("FlashAttention-4反向传播优化" section 1.1; "FlashAttention-2-
+ * ICLR24" 核心方法 2: parallel over key/value blocks, dQ merged across blocks).
+ *   q, k, v, dout: device bf16 as in fa_fwd.  lse, D: device fp32 [Hq,T] from
+ *   fa_fwd and fa_bwd_preprocess.
+ *   dq [T,Hq,d], dk/dv [T,Hkv,d]: device, written in grad_dtype.
+ *   workspace: the one fa_bwd_preprocess just reset, same sizes and flags.
+ *   deterministic = 0: dQ partials are added with fp32 atomics (fast, the
+ *   summation order varies run to run).  deterministic = 1: each dQ tile's
+ *   partials are added in a fixed order serialised by semaphores
+ *   ("FlashAttention-4反向传播优化" section 3.2), so repeated runs give
+ *   bit-identical dq/dk/dv.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout, const float* lse,
+                 const float* D, void* dq, void* dk, void* dv, fa_dtype grad_dtype,
+                 void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N,
+                 int total_tokens, int d, float scale, int causal, const int* cu_seqlens,
+                 int deterministic, fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads the device error word of a backward or
+ * forward workspace: FA_OK, FA_ERR_TIMEOUT (a bounded wait gave up),
+ * FA_ERR_INVALID_ARG (a sequence longer than N), or FA_ERR_CUDA if
+ * synchronisation or the read failed.
+ */
+fa_status fa_check_device_status(const void* workspace, fa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,130 @@
+"""The C-ABI library: it builds, loads, exports every symbol include/fa.h
+declares, and rejects bad arguments on the host (no GPU needed: validation
+returns before any CUDA call)."""
+import os
+import re
+
+import pytest
+
+import bwd_tiled_attention_gb300 as fa
+from bwd_tiled_attention_gb300 import build as fabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    fabuild.build()
+    return fa.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_bwd" in names and "fa_bwd_preprocess" in names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(fa.EXPORTED)
+
+
+def test_status_strings(L):
+    assert fa.fa_status_string(0) == "FA_OK"
+    assert fa.fa_status_string(4) == "FA_ERR_TIMEOUT"
+    assert L.fa_version().decode().startswith("gb300")
+
+
+def test_workspace_sizes(L):
+    # forward: header + unit list, grows with heads and tokens
+    a = fa.fa_fwd_workspace_size(4, 16, 2048, 0)
+    b = fa.fa_fwd_workspace_size(4, 32, 2048, 0)
+    assert 0 < a < b
+    # backward: includes the fp32 dQ accumulator [T, Hq, d]
+    T, Hq, d = 4 * 2048, 16, 128
+    w = fa.fa_bwd_workspace_size(4, Hq, Hq, 2048, 0, d)
+    assert w >= T * Hq * d * 4
+    # GQA adds fp32 dK and dV partials per query head
+    wg = fa.fa_bwd_workspace_size(4, Hq, 4, 2048, 0, d)
+    assert wg >= w + 2 * T * Hq * d * 4
+    off = fa.fa_bwd_workspace_semaphore_offset(4, Hq, Hq, 2048, 0, d)
+    assert 0 < off < w and off % 256 == 0
+    assert fa.fa_bwd_workspace_size(1, 4, 4, 16, 0, 96) == 0   # unsupported head dim
+
+
+FAKE = 0x10000          # 16-byte aligned non-null fake device address (never dereferenced)
+
+
+def fwd_call(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, o_dtype=fa.FA_BF16, lse=FAKE, B=2, Hq=4, Hkv=2,
+                N=64, total_tokens=0, d=64, scale=0.125, causal=1, cu_seqlens=None,
+                workspace=FAKE, workspace_bytes=1 << 20, stream=0)
+    args.update(kw)
+    return fa.fa_fwd(**args)
+
+
+def test_fwd_rejects_bad_arguments(L):
+    assert fwd_call(Hkv=3) == fa.FA_ERR_INVALID_ARG            # Hq % Hkv != 0
+    assert fwd_call(d=96) == fa.FA_ERR_UNSUPPORTED              # head dim
+    assert fwd_call(q=FAKE + 8) == fa.FA_ERR_INVALID_ARG        # TMA needs 16-byte alignment
+    assert fwd_call(lse=None) == fa.FA_ERR_INVALID_ARG          # null output
+    assert fwd_call(workspace_bytes=8) == fa.FA_ERR_INVALID_ARG
+    assert fwd_call(scale=0.0) == fa.FA_ERR_UNSUPPORTED
+    assert fwd_call(scale=float("nan")) == fa.FA_ERR_UNSUPPORTED
+    assert fwd_call(total_tokens=100) == fa.FA_ERR_INVALID_ARG  # dense T must be B*N
+    assert fwd_call(o_dtype=7) == fa.FA_ERR_INVALID_ARG
+    assert fwd_call(B=-1) == fa.FA_ERR_INVALID_ARG
+    assert fwd_call(B=5000, cu_seqlens=FAKE, total_tokens=10) == fa.FA_ERR_UNSUPPORTED
+    assert fwd_call(cu_seqlens=FAKE + 2, total_tokens=10) == fa.FA_ERR_INVALID_ARG
+
+
+def test_empty_inputs_are_a_no_op(L):
+    # nothing to compute: success without touching the device
+    assert fwd_call(B=0, N=0) == fa.FA_OK
+    assert fwd_call(N=0) == fa.FA_OK
+    assert fwd_call(cu_seqlens=FAKE, total_tokens=0) == fa.FA_OK
+
+
+def bwd_call(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, dout=FAKE, lse=FAKE, D=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+                grad_dtype=fa.FA_BF16, workspace=FAKE, workspace_bytes=1 << 30, B=2, Hq=4, Hkv=2,
+                N=64, total_tokens=0, d=128, scale=0.1, causal=0, cu_seqlens=None,
+                deterministic=1, stream=0)
+    args.update(kw)
+    return fa.fa_bwd(**args)
+
+
+def test_bwd_rejects_bad_arguments(L):
+    assert bwd_call(Hkv=3) == fa.FA_ERR_INVALID_ARG
+    assert bwd_call(d=32) == fa.FA_ERR_UNSUPPORTED
+    assert bwd_call(dk=FAKE + 4) == fa.FA_ERR_INVALID_ARG
+    assert bwd_call(D=None) == fa.FA_ERR_INVALID_ARG
+    assert bwd_call(workspace_bytes=1024) == fa.FA_ERR_INVALID_ARG
+    assert bwd_call(grad_dtype=3) == fa.FA_ERR_INVALID_ARG
+    assert bwd_call(scale=-1.0) == fa.FA_ERR_UNSUPPORTED
+    assert bwd_call(B=0) == fa.FA_OK
+    pre = dict(o=FAKE, o_dtype=fa.FA_BF16, dout=FAKE, D=FAKE, workspace=FAKE,
+               workspace_bytes=1 << 30, B=2, Hq=4, Hkv=2, N=64, total_tokens=0, d=128, causal=1,
+               cu_seqlens=None, deterministic=0, stream=0)
+    assert fa.fa_bwd_preprocess(**dict(pre, Hq=5)) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_preprocess(**dict(pre, dout=FAKE + 2)) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_preprocess(**dict(pre, workspace_bytes=64)) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_preprocess(**dict(pre, o_dtype=9)) == fa.FA_ERR_INVALID_ARG
+
+
+def test_check_status_null(L):
+    assert fa.fa_check_device_status(None, 0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_product_package_does_not_import_oracle():
+    """The product path never reaches the oracle (no CPU fallback)."""
+    pkg = os.path.join(ROOT, "bwd_tiled_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f

@@ -1,0 +1,119 @@
+"""GPU parity against the fp64 oracle on sizes the oracle finishes in seconds:
+several tiles, ragged tails, packed variable-length batches, GQA/MQA, head
+dims 64 and 128, causal and not.  Every call goes through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import bwd_tiled_attention_gb300 as fa
+import oracle
+import synth
+from harness import assert_close, assert_lse, cuda_inputs, oracle_inputs, to_np
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # name, lengths, Hq, Hkv, d
+    ("tiny_d64", [128], 2, 2, 64),
+    ("ragged_300", [300, 300], 4, 4, 128),
+    ("varlen_edges", [1, 127, 128, 129, 255, 256, 257, 600], 4, 2, 128),
+    ("varlen_d64_mqa", [5, 200, 384, 70], 6, 1, 64),
+    ("gqa4_512", [512, 512], 8, 2, 128),
+]
+
+
+def run_case(lengths, Hq, Hkv, d, causal, seed=11, o_fp32=False, deterministic=False):
+    inp = synth.make_inputs(B=len(lengths), Hq=Hq, Hkv=Hkv, d=d, seed=seed, lengths=lengths)
+    scale = 1.0 / np.sqrt(d)
+    oi = oracle_inputs(inp)
+    ref = oracle.attention(oi["q"], oi["k"], oi["v"], inp["cu_seqlens"].numpy(), scale, causal,
+                           dout=oi["dout"])
+    x = cuda_inputs(inp)
+    N = max(lengths)
+    o, lse = fa.forward(x["q"], x["k"], x["v"], causal=causal, scale=scale,
+                        cu_seqlens=x["cu_seqlens"], max_seqlen=N,
+                        out_dtype=torch.float32 if o_fp32 else torch.bfloat16)
+    dq, dk, dv = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=causal,
+                             scale=scale, cu_seqlens=x["cu_seqlens"], max_seqlen=N,
+                             deterministic=deterministic, check_status=True)
+    torch.cuda.synchronize()
+    return ref, dict(o=to_np(o), lse=to_np(lse), dq=to_np(dq), dk=to_np(dk), dv=to_np(dv))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("name,lengths,Hq,Hkv,d", CASES)
+def test_forward_backward_parity(name, lengths, Hq, Hkv, d, causal):
+    ref, got = run_case(lengths, Hq, Hkv, d, causal)
+    assert_close("o", got["o"], ref["o"])
+    assert_lse(got["lse"], ref["lse"])
+    assert_close("dq", got["dq"], ref["dq"])
+    assert_close("dk", got["dk"], ref["dk"])
+    assert_close("dv", got["dv"], ref["dv"])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_deterministic_mode_parity(causal):
+    ref, got = run_case([129, 300, 77, 512], 4, 2, 128, causal, seed=5, deterministic=True)
+    for name in ("dq", "dk", "dv"):
+        assert_close(name, got[name], ref[name])
+
+
+def test_tiny_config_fp32_output():
+    """B=1, Hq=Hkv=2, N=128, d=64, non-causal, seed 0, fp32 O and LSE."""
+    w = synth.workloads()["tiny"]
+    inp = synth.make_workload(w)
+    oi = oracle_inputs(inp)
+    ref = oracle.attention(oi["q"], oi["k"], oi["v"], inp["cu_seqlens"].numpy(), w.scale,
+                           w.causal, dout=oi["dout"])
+    x = cuda_inputs(inp)
+    o, lse = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, batch=w.B,
+                        out_dtype=torch.float32)
+    assert o.dtype == torch.float32
+    dq, dk, dv = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=w.causal,
+                             scale=w.scale, batch=w.B, check_status=True)
+    assert_close("o", to_np(o), ref["o"], rel=2e-3, mabs=2e-3)   # fp32 output: tighter
+    assert_lse(to_np(lse), ref["lse"])
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert_close(name, to_np(t), ref[name])
+
+
+def test_fp32_gradients():
+    ref, _ = run_case([300], 4, 4, 128, True, seed=21)
+    inp = synth.make_inputs(B=1, Hq=4, Hkv=4, d=128, seed=21, lengths=[300])
+    x = cuda_inputs(inp)
+    o, lse = fa.forward(x["q"], x["k"], x["v"], causal=True, batch=1)
+    g = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=True, batch=1,
+                    grad_dtype=torch.float32, check_status=True)
+    for name, t in zip(("dq", "dk", "dv"), g):
+        assert t.dtype == torch.float32
+        assert_close(name, to_np(t), ref[name])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_deterministic_bit_identical_small(causal):
+    lengths = [129, 300, 77, 512]
+    inp = synth.make_inputs(B=4, Hq=4, Hkv=2, d=128, seed=5, lengths=lengths)
+    x = cuda_inputs(inp)
+    o, lse = fa.forward(x["q"], x["k"], x["v"], causal=causal, cu_seqlens=x["cu_seqlens"],
+                        max_seqlen=512)
+    first = None
+    for _ in range(5):
+        g = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=causal,
+                        cu_seqlens=x["cu_seqlens"], max_seqlen=512, deterministic=True,
+                        check_status=True)
+        g = [t.clone() for t in g]
+        if first is None:
+            first = g
+        else:
+            for a, b in zip(first, g):
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_dense_batch_equals_varlen_packing():
+    """A dense batch and the same tokens described by cu_seqlens agree bit for bit."""
+    inp = synth.make_inputs(B=3, Hq=4, Hkv=4, d=128, seed=9, N=384)
+    x = cuda_inputs(inp)
+    o1, l1 = fa.forward(x["q"], x["k"], x["v"], causal=True, batch=3)
+    o2, l2 = fa.forward(x["q"], x["k"], x["v"], causal=True, cu_seqlens=x["cu_seqlens"],
+                        max_seqlen=384)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
