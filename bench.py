@@ -1,0 +1,364 @@
+"""Benchmark: tiled attention forward + backward on GB300.
+
+One step = forward (fa_fwd) + backward (fa_bwd_preprocess + fa_bwd) of the
+whole workload, with inputs resident in HBM and the L2 flushed before every
+step (a 512 MB write outside the step's events).  Throughput counts the
+algorithmic FLOPs 4*B*Hq*N^2*d (forward) and 2.5x that (backward), halved for
+causal; a packed variable-length batch uses sum(L_b^2) for B*N^2.
+
+Default workload: B=4, Hq=Hkv=16, N=2048, d=128, causal, bf16, seeded N(0,1)
+inputs (the mid-size dense configuration, causal).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+work partitions by batch/head with no exchange); the job value is the sum of
+the ranks' FLOPs over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402  (input generator: no attention arithmetic)
+
+METRIC = "attention fwd+bwd BF16 TFLOPs/s (hd128, causal) and % of GB300 dense BF16 peak"
+NOMINAL_PEAK_TFLOPS = 2250.0
+
+
+def workload_flops(w, lengths):
+    sq = sum(L * L for L in lengths)
+    fwd = 4.0 * w.Hq * sq * w.d
+    if w.causal:
+        fwd /= 2.0
+    return fwd, 2.5 * fwd
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return None
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(w, inp, budget_s=12.0):
+    """The fp64 oracle on the host cores over a bounded sample of the workload:
+    whole (sequence, head) problems, forward + backward, until ~budget_s."""
+    import numpy as np
+
+    import oracle
+
+    def f64(t):
+        return t.float().numpy().astype(np.float64)
+
+    q, k, v, do = (f64(inp[x]) for x in ("q", "k", "v", "dout"))
+    cu = inp["cu_seqlens"].numpy()
+    lengths = inp["lengths"]
+    done_flops, heads = 0.0, 0
+    grp = w.Hq // w.Hkv
+    t0 = time.perf_counter()
+    for b in range(len(lengths)):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        for h in range(w.Hq):
+            g = h // grp
+            oracle.attention(q[s0:s1, h:h + 1], k[s0:s1, g:g + 1], v[s0:s1, g:g + 1],
+                             [0, s1 - s0], w.scale, w.causal, dout=do[s0:s1, h:h + 1])
+            f, bw = workload_flops(w, [s1 - s0])
+            done_flops += (f + bw) / w.Hq
+            heads += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{heads} (sequence, head) problems of the workload, fwd+bwd in fp64, "
+                      f"{dt:.1f} s"}
+
+
+def config_of(w, inp, world):
+    lengths = inp["lengths"]
+    return {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} "
+                        f"N={max(lengths)} d={w.d} {'causal' if w.causal else 'non-causal'}"
+                        f"{' deterministic' if w.deterministic else ''}",
+            "global_batch": w.B * world, "seq_len": max(lengths), "tokens": sum(lengths) * world,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed before every step (512 MB write, outside the step events)"}
+
+
+def run_reference(args, w, inp, rank, world):
+    if rank != 0:
+        return 0
+    K, W = args.steps, args.warmup
+    for _ in range(min(W, 1)):
+        cpu_baseline(w, inp, budget_s=1.0)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(K):
+        vals.append(cpu_baseline(w, inp, budget_s=args.ref_step_s))
+    wall = time.perf_counter() - t0
+    value = statistics.mean(v["value"] for v in vals)
+    flops_step = sum(workload_flops(w, inp["lengths"]))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": flops_step / (value * 1e12) * 1e3 if value > 0 else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), bf16-rounded)", "config": config_of(w, inp, world),
+        "cpu_baseline": dict(vals[-1], value=value),
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mid_causal", choices=sorted(synth.workloads()))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = synth.workloads()[args.workload]
+    inp = synth.make_workload(w)
+
+    if args.impl == "reference":
+        return run_reference(args, w, inp, rank, world)
+
+    import torch
+
+    import bwd_tiled_attention_gb300 as fa
+    from bwd_tiled_attention_gb300 import build as fabuild
+    fabuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    lengths = inp["lengths"]
+    B, Hq, Hkv, d = w.B, w.Hq, w.Hkv, w.d
+    N, T = max(lengths), sum(lengths)
+    scale = w.scale
+    varlen = w.len_range is not None
+    x = {k: inp[k].to(dev) for k in ("q", "k", "v", "dout")}
+    cu = inp["cu_seqlens"].to(dev) if varlen else None
+    o = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    Dv = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(x["q"])
+    dk = torch.empty_like(x["k"])
+    dv = torch.empty_like(x["v"])
+    fws_b = fa.fa_fwd_workspace_size(B, Hq, N, T)
+    bws_b = fa.fa_bwd_workspace_size(B, Hq, Hkv, N, T, d)
+    fws = torch.empty(fws_b, dtype=torch.uint8, device=dev)
+    bws = torch.empty(bws_b, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    det = bool(w.deterministic)
+
+    def check(st, what):
+        if st != fa.FA_OK:
+            raise fa.FAError(st, what)
+
+    def step(events=None):
+        if events:
+            events[0].record(stream)
+        check(fa.fa_fwd(x["q"], x["k"], x["v"], o, fa.FA_BF16, lse, B, Hq, Hkv, N, T, d, scale,
+                        w.causal, cu, fws, fws_b, stream), "fa_fwd")
+        if events:
+            events[1].record(stream)
+        check(fa.fa_bwd_preprocess(o, fa.FA_BF16, x["dout"], Dv, bws, bws_b, B, Hq, Hkv, N, T, d,
+                                   w.causal, cu, det, stream), "fa_bwd_preprocess")
+        if events:
+            events[2].record(stream)
+        check(fa.fa_bwd(x["q"], x["k"], x["v"], x["dout"], lse, Dv, dq, dk, dv, fa.FA_BF16, bws,
+                        bws_b, B, Hq, Hkv, N, T, d, scale, w.causal, cu, det, stream), "fa_bwd")
+        if events:
+            events[3].record(stream)
+
+    launches_per_step = 6  # scheduler + fwd, scheduler + preprocess, bwd + postprocess
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    check(fa.fa_check_device_status(bws, stream), "device status")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    check(fa.fa_check_device_status(bws, stream), "device status")
+    t_fwd = [e[0].elapsed_time(e[1]) for e in evs]
+    t_pre = [e[1].elapsed_time(e[2]) for e in evs]
+    t_bwd = [e[2].elapsed_time(e[3]) for e in evs]
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(t_step)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    fl_f, fl_b = workload_flops(w, lengths)
+    value = (fl_f + fl_b) * K * world / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / K
+
+    # end to end through the public API with host buffers: H2D inputs, fwd+bwd, D2H grads
+    host_in = {k: inp[k].pin_memory() for k in ("q", "k", "v", "dout")}
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    E = args.e2e_steps
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for i in range(E + 2):
+        if i == 2:
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            e0.record(stream)
+        for k_ in ("q", "k", "v", "dout"):
+            x[k_].copy_(host_in[k_], non_blocking=True)
+        step()
+        for src, dst in zip((dq, dk, dv), host_out):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = (fl_f + fl_b) * E * world / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_kind = measured_peaks()
+    bwd_call_ms = statistics.mean(t_bwd)
+    achieved = fl_b / (bwd_call_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": config_of(w, inp, world),
+        "pct_of_nominal_peak": 100.0 * value / world / NOMINAL_PEAK_TFLOPS,
+        "pct_of_measured_peak": 100.0 * value / world / peak,
+        "breakdown": {
+            "fwd_ms": statistics.mean(t_fwd), "bwd_preprocess_ms": statistics.mean(t_pre),
+            "bwd_ms": bwd_call_ms,
+            "fwd_tflops": fl_f / (statistics.mean(t_fwd) * 1e-3) / 1e12,
+            "bwd_tflops_incl_preprocess": fl_b / ((statistics.mean(t_pre) + bwd_call_ms) * 1e-3)
+            / 1e12,
+        },
+        "roofline": {"bound": "tensor", "kernel": "fa_bwd (backward kernel + dQ conversion)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} bf16 burst",
+                     "traffic": None},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
