@@ -26,12 +26,28 @@ def errors(got: np.ndarray, ref: np.ndarray):
     return float(rel), float(np.max(np.abs(diff))) if diff.size else 0.0
 
 
-def assert_close(name, got, ref, rel=REL_FROB, mabs=MAX_ABS):
+def bf16_half_ulp(x):
+    """Half the spacing of bfloat16 (8 significant bits) at |x|: the error that
+    rounding an exact value to bf16 for storage may add on its own."""
+    ax = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 8)
+
+
+def assert_close(name, got, ref, rel=REL_FROB, mabs=MAX_ABS, stored_bf16=True):
+    """Relative Frobenius error <= rel and max-abs error <= mabs.
+
+    For outputs stored as bf16 the max-abs check discounts, element by element,
+    the bf16 storage rounding of the reference value (half an ulp: 2^-5 for
+    |x| in [8, 16)), which alone can exceed 2e-2; the same kernels' fp32
+    outputs are checked without that allowance."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     r, m = errors(got, ref)
-    assert r <= rel and m <= mabs, (
-        f"{name}: rel_frob={r:.3e} max_abs={m:.3e} (max|ref|={np.max(np.abs(ref)):.3g})")
+    slack = bf16_half_ulp(ref) if stored_bf16 else 0.0
+    excess = float(np.max(np.abs(got - ref) - slack)) if got.size else 0.0
+    assert r <= rel and excess <= mabs, (
+        f"{name}: rel_frob={r:.3e} max_abs={m:.3e} beyond-storage={excess:.3e} "
+        f"(max|ref|={np.max(np.abs(ref)):.3g})")
     return r, m
 
 

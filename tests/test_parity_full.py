@@ -1,0 +1,137 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+benchmark times, against the fp64 oracle on sampled outputs.
+
+The oracle computes O, LSE and dQ of one row from that row alone, and dK, dV of
+a key from the rows that see it, so samples cost O(L*d) per row.  Each test
+samples rows across heads and sequences, keys from the last part of the
+sequence (cheap under the causal mask), and whole heads where that fits in a
+few seconds.  The deterministic backward must also be bit-identical over 10
+runs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bwd_tiled_attention_gb300 as fa
+import oracle
+import synth
+from harness import assert_close, assert_lse, cuda_inputs, oracle_inputs, to_np
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def run_gpu(w, inp, deterministic=None, grad_dtype=torch.bfloat16):
+    x = cuda_inputs(inp)
+    varlen = w.len_range is not None
+    N = max(inp["lengths"])
+    kw = dict(cu_seqlens=x["cu_seqlens"], max_seqlen=N) if varlen else dict(batch=w.B)
+    det = w.deterministic if deterministic is None else deterministic
+    o, lse = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, **kw)
+    dq, dk, dv = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=w.causal,
+                             scale=w.scale, deterministic=det, grad_dtype=grad_dtype,
+                             check_status=True, **kw)
+    torch.cuda.synchronize()
+    return x, dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+def check_rows(w, inp, got, samples, rng, nrows=24, stored_bf16=True):
+    """samples: list of (b, h).  Compares O, LSE, dQ on random rows."""
+    oi = oracle_inputs(inp)
+    cu = inp["cu_seqlens"].numpy()
+    for b, h in samples:
+        L = int(cu[b + 1] - cu[b])
+        rows = np.unique(np.concatenate([[0, L - 1], rng.integers(0, L, nrows)]))
+        ref = oracle.rows(oi["q"], oi["k"], oi["v"], cu, w.scale, w.causal, b, h, rows,
+                          dout=oi["dout"])
+        t = cu[b] + rows
+        assert_close(f"o b{b} h{h}", to_np(got["o"][t, h]), ref["o"])
+        assert_lse(to_np(got["lse"][h, t]), ref["lse"])
+        assert_close(f"dq b{b} h{h}", to_np(got["dq"][t, h]), ref["dq"], stored_bf16=stored_bf16)
+
+
+def check_keys(w, inp, got, samples, rng, lo_frac=0.75, nkeys=24, stored_bf16=True):
+    """samples: list of (b, g).  Compares dK, dV on random keys of the last part."""
+    oi = oracle_inputs(inp)
+    cu = inp["cu_seqlens"].numpy()
+    for b, g in samples:
+        L = int(cu[b + 1] - cu[b])
+        lo = int(L * lo_frac)
+        keys = np.unique(np.concatenate([[lo, L - 1], rng.integers(lo, L, nkeys)]))
+        ref = oracle.key_grads(oi["q"], oi["k"], oi["v"], oi["dout"], cu, w.scale, w.causal, b, g,
+                               keys)
+        t = cu[b] + keys
+        assert_close(f"dk b{b} g{g}", to_np(got["dk"][t, g]), ref["dk"], stored_bf16=stored_bf16)
+        assert_close(f"dv b{b} g{g}", to_np(got["dv"][t, g]), ref["dv"], stored_bf16=stored_bf16)
+
+
+def check_whole_head(w, inp, got, b, h):
+    """Every output of one (sequence, head) of an MHA workload."""
+    assert w.Hq == w.Hkv
+    oi = oracle_inputs(inp)
+    cu = inp["cu_seqlens"].numpy()
+    s0, s1 = int(cu[b]), int(cu[b + 1])
+    sl = lambda a: a[s0:s1, h:h + 1]
+    ref = oracle.attention(sl(oi["q"]), sl(oi["k"]), sl(oi["v"]), [0, s1 - s0], w.scale,
+                           w.causal, dout=sl(oi["dout"]))
+    for name in ("o", "dq", "dk", "dv"):
+        assert_close(f"{name} b{b} h{h}", to_np(got[name][s0:s1, h]), ref[name][:, 0])
+    assert_lse(to_np(got["lse"][h, s0:s1]), ref["lse"][0])
+
+
+@pytest.mark.parametrize("name", ["mid_dense", "mid_causal"])
+def test_mid(name):
+    w = synth.workloads()[name]
+    inp = synth.make_workload(w)
+    _, got = run_gpu(w, inp)
+    rng = np.random.default_rng(1)
+    check_whole_head(w, inp, got, 0, 0)
+    check_whole_head(w, inp, got, 3, 15)
+    check_rows(w, inp, got, [(1, 7), (2, 3)], rng)
+    check_keys(w, inp, got, [(1, 9)], rng, lo_frac=0.8 if w.causal else 0.0, nkeys=8)
+
+
+def test_long_causal():
+    w = synth.workloads()["long_causal"]
+    inp = synth.make_workload(w)
+    _, got = run_gpu(w, inp)
+    rng = np.random.default_rng(2)
+    check_rows(w, inp, got, [(0, 0), (0, 1)], rng, nrows=32)
+    check_keys(w, inp, got, [(0, 0), (0, 1)], rng, lo_frac=0.85, nkeys=24)
+
+
+@pytest.mark.parametrize("name", ["gqa8_causal", "mqa_causal"])
+def test_grouped(name):
+    w = synth.workloads()[name]
+    inp = synth.make_workload(w)
+    _, got = run_gpu(w, inp)
+    rng = np.random.default_rng(3)
+    check_rows(w, inp, got, [(0, 0), (0, w.Hq - 1), (1, w.Hq // 2)], rng)
+    check_keys(w, inp, got, [(0, 0), (1, w.Hkv - 1)], rng, lo_frac=0.9, nkeys=16)
+    # fp32 gradient outputs: the strict bound, no storage rounding
+    _, g32 = run_gpu(w, inp, grad_dtype=torch.float32)
+    rng = np.random.default_rng(3)
+    check_rows(w, inp, g32, [(0, 0), (0, w.Hq - 1)], rng, stored_bf16=False)
+    check_keys(w, inp, g32, [(0, 0)], rng, lo_frac=0.9, nkeys=16, stored_bf16=False)
+
+
+def test_varlen_deterministic():
+    w = synth.workloads()["varlen_det"]
+    inp = synth.make_workload(w)
+    x, got = run_gpu(w, inp)
+    rng = np.random.default_rng(4)
+    B = len(inp["lengths"])
+    shortest = int(np.argmin(inp["lengths"]))
+    check_whole_head(w, inp, got, shortest, 5)
+    check_rows(w, inp, got, [(b, int(rng.integers(0, w.Hq))) for b in range(0, B, 3)], rng,
+               nrows=12)
+    check_keys(w, inp, got, [(b, int(rng.integers(0, w.Hkv))) for b in (0, B - 1)], rng,
+               lo_frac=0.8, nkeys=12)
+    # bit-identical over 10 runs of the deterministic backward
+    N = max(inp["lengths"])
+    ref = [got[k].clone() for k in ("dq", "dk", "dv")]
+    for _ in range(10):
+        g = fa.backward(x["q"], x["k"], x["v"], got["o"], x["dout"], got["lse"], causal=True,
+                        scale=w.scale, cu_seqlens=x["cu_seqlens"], max_seqlen=N,
+                        deterministic=True, check_status=True)
+        for a, b_ in zip(ref, g):
+            assert torch.equal(a.view(torch.int16), b_.view(torch.int16))

@@ -36,8 +36,14 @@ def run_case(lengths, Hq, Hkv, d, causal, seed=11, o_fp32=False, deterministic=F
     dq, dk, dv = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=causal,
                              scale=scale, cu_seqlens=x["cu_seqlens"], max_seqlen=N,
                              deterministic=deterministic, check_status=True)
+    got = dict(o=to_np(o), lse=to_np(lse), dq=to_np(dq), dk=to_np(dk), dv=to_np(dv))
+    # the same backward with fp32 gradient outputs (no bf16 storage rounding)
+    g32 = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=causal, scale=scale,
+                      cu_seqlens=x["cu_seqlens"], max_seqlen=N, deterministic=deterministic,
+                      grad_dtype=torch.float32, check_status=True)
     torch.cuda.synchronize()
-    return ref, dict(o=to_np(o), lse=to_np(lse), dq=to_np(dq), dk=to_np(dk), dv=to_np(dv))
+    got.update({n + "32": to_np(t) for n, t in zip(("dq", "dk", "dv"), g32)})
+    return ref, got
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -46,9 +52,9 @@ def test_forward_backward_parity(name, lengths, Hq, Hkv, d, causal):
     ref, got = run_case(lengths, Hq, Hkv, d, causal)
     assert_close("o", got["o"], ref["o"])
     assert_lse(got["lse"], ref["lse"])
-    assert_close("dq", got["dq"], ref["dq"])
-    assert_close("dk", got["dk"], ref["dk"])
-    assert_close("dv", got["dv"], ref["dv"])
+    for g in ("dq", "dk", "dv"):
+        assert_close(g, got[g], ref[g])
+        assert_close(g + " (fp32 out)", got[g + "32"], ref[g], stored_bf16=False)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -56,6 +62,7 @@ def test_deterministic_mode_parity(causal):
     ref, got = run_case([129, 300, 77, 512], 4, 2, 128, causal, seed=5, deterministic=True)
     for name in ("dq", "dk", "dv"):
         assert_close(name, got[name], ref[name])
+        assert_close(name + " (fp32 out)", got[name + "32"], ref[name], stored_bf16=False)
 
 
 def test_tiny_config_fp32_output():
@@ -71,7 +78,7 @@ def test_tiny_config_fp32_output():
     assert o.dtype == torch.float32
     dq, dk, dv = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=w.causal,
                              scale=w.scale, batch=w.B, check_status=True)
-    assert_close("o", to_np(o), ref["o"], rel=2e-3, mabs=2e-3)   # fp32 output: tighter
+    assert_close("o", to_np(o), ref["o"], rel=2e-3, mabs=2e-3, stored_bf16=False)
     assert_lse(to_np(lse), ref["lse"])
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         assert_close(name, to_np(t), ref[name])
@@ -86,7 +93,7 @@ def test_fp32_gradients():
                     grad_dtype=torch.float32, check_status=True)
     for name, t in zip(("dq", "dk", "dv"), g):
         assert t.dtype == torch.float32
-        assert_close(name, to_np(t), ref[name])
+        assert_close(name, to_np(t), ref[name], stored_bf16=False)
 
 
 @pytest.mark.parametrize("causal", [False, True])
