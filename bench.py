@@ -44,6 +44,29 @@ def workload_flops(w, lengths):
     return fwd, 2.5 * fwd
 
 
+def job_throughput(flops_per_rank, elapsed_ms, dist=None, device=None):
+    """Whole-job TFLOP/s: every rank's FLOPs over the slowest rank's time.
+
+    With torch.distributed initialised the elapsed time is max-reduced over the
+    ranks (the only cross-rank traffic of the benchmark; the attention work
+    itself partitions with no exchange).  Returns (tflops, max_elapsed_ms)."""
+    world = 1
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        t = torch.tensor([float(elapsed_ms)], dtype=torch.float64,
+                         device=device if device is not None else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        f = torch.tensor([float(flops_per_rank)], dtype=torch.float64,
+                         device=device if device is not None else "cpu")
+        dist.all_reduce(f, op=dist.ReduceOp.SUM)
+        total = float(f.item())
+    else:
+        total = float(flops_per_rank) * world
+    return total / (elapsed_ms * 1e-3) / 1e12, elapsed_ms
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -286,13 +309,8 @@ def main():
     t_pre = [e[1].elapsed_time(e[2]) for e in evs]
     t_bwd = [e[2].elapsed_time(e[3]) for e in evs]
     t_step = [e[0].elapsed_time(e[3]) for e in evs]
-    total_ms = sum(t_step)
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
     fl_f, fl_b = workload_flops(w, lengths)
-    value = (fl_f + fl_b) * K * world / (total_ms * 1e-3) / 1e12
+    value, total_ms = job_throughput((fl_f + fl_b) * K, sum(t_step), dist, dev)
     ms_per_step = total_ms / K
 
     # end to end through the public API with host buffers: H2D inputs, fwd+bwd, D2H grads
@@ -316,12 +334,7 @@ def main():
             dst.copy_(src, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = (fl_f + fl_b) * E * world / (e2e_ms * 1e-3) / 1e12
+    e2e_value, _ = job_throughput((fl_f + fl_b) * E, e0.elapsed_time(e1), dist, dev)
 
     peaks, peak_kind = measured_peaks()
     bwd_call_ms = statistics.mean(t_bwd)
