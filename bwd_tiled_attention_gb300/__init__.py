@@ -27,6 +27,7 @@ from . import build as _build
 __all__ = [
     "FAError", "lib", "fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_fwd_workspace_size",
     "fa_bwd_workspace_size", "fa_bwd_workspace_semaphore_offset", "fa_check_device_status",
+    "fa_bwd_noalloc",
     "fa_status_string", "forward", "backward", "attention", "FA_OK", "FA_ERR_INVALID_ARG",
     "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_BF16", "FA_FP32",
 ]
@@ -55,6 +56,8 @@ _SIGS = {
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _i, _i, _i, _i, _i,
                     _i, _f, _i, _vp, _i, _vp]),
     "fa_check_device_status": (_i, [_vp, _vp]),
+    "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                            _i, _i, _f, _i, _vp, _i, _vp]),
 }
 
 EXPORTED = tuple(_SIGS)
@@ -157,6 +160,15 @@ def fa_bwd(q, k, v, dout, lse, D, dq, dk, dv, grad_dtype, workspace, workspace_b
                             int(workspace_bytes), B, Hq, Hkv, N, total_tokens, d, float(scale),
                             int(bool(causal)), _ptr(cu_seqlens), int(bool(deterministic)),
                             _stream(stream)))
+
+
+def fa_bwd_noalloc(q, k, v, o, o_dtype, dout, lse, dq, dk, dv, grad_dtype, B, Hq, Hkv, N,
+                   total_tokens, d, scale, causal, cu_seqlens, deterministic, stream=None) -> int:
+    """Backward without a caller workspace (library-owned 64 MiB scratch); see include/fa.h."""
+    return int(lib().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o_dtype), _ptr(dout),
+                                    _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _dt(grad_dtype), B,
+                                    Hq, Hkv, N, total_tokens, d, float(scale), int(bool(causal)),
+                                    _ptr(cu_seqlens), int(bool(deterministic)), _stream(stream)))
 
 
 def fa_check_device_status(workspace, stream=None) -> int:

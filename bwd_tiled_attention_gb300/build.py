@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfa_gb300.so")
-SOURCES = ["api.cu", "sched.cu", "fwd.cu", "bwd.cu"]
+SOURCES = ["api.cu", "sched.cu", "fwd.cu", "bwd.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "internal.h", "sm100_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

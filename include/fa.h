@@ -19,7 +19,8 @@
  * --------------------------------
  * - Pointers marked "device" are CUDA device pointers; the caller allocates
  *   and owns every buffer, including the workspaces.  The library allocates
- *   nothing and keeps no state besides cached device attributes.
+ *   nothing and keeps no state besides cached device attributes (and the
+ *   fixed scratch array that fa_bwd_noalloc uses, described there).
  * - Token-major packed layouts, head dim innermost and contiguous:
  *     q, o, dout, dq : [T, Hq, d]      k, v, dk, dv : [T, Hkv, d]
  *     lse, D         : [Hq, T] fp32
@@ -150,6 +151,34 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout, 
                  void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N,
                  int total_tokens, int d, float scale, int causal, const int* cu_seqlens,
                  int deterministic, fa_stream_t stream);
+
+/*
+ * Backward pass for callers that cannot allocate device memory: same inputs,
+ * outputs and results as fa_bwd_preprocess followed by fa_bwd, but D and the
+ * backward workspace live in a 64 MiB scratch array owned by the library, so
+ * the caller passes no workspace.  The pages have no counterpart of this call;
+ * it exists for code that runs where allocation is not allowed (an engine
+ * plugin whose execute step must not allocate, a process whose device memory
+ * is all reserved up front) and that has no buffer of its own to lend.
+ *   Inputs q, k, v, o (o_dtype), dout, lse and outputs dq, dk, dv (grad_dtype)
+ *   are as in fa_fwd / fa_bwd; o and lse come from fa_fwd.
+ *   Limit: fa_bwd_workspace_size(B,Hq,Hkv,N,total_tokens,d) plus 4*Hq*T bytes
+ *   (rounded up to 256) must fit in 64 MiB; larger requests return
+ *   FA_ERR_UNSUPPORTED and launch nothing.
+ *   Every GPU that loads the library holds the 64 MiB until the process
+ *   exits.  The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  The call allocates nothing.
+ *   All calls share the one array, which keeps the last call's contents (the
+ *   parts that must start at zero are cleared on every call): calls that can
+ *   overlap on the GPU -- on different streams, or from different host
+ *   threads -- race on it and must be serialised by the caller.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         fa_dtype o_dtype, const void* dout, const float* lse, void* dq, void* dk,
+                         void* dv, fa_dtype grad_dtype, int B, int Hq, int Hkv, int N,
+                         int total_tokens, int d, float scale, int causal, const int* cu_seqlens,
+                         int deterministic, fa_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads the device error word of a backward or
