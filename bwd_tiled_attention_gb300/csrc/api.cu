@@ -66,6 +66,21 @@ bool make_map(CUtensorMap* m, const void* base, int T, int H, int d) {
     return r == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over the packed [T, H, d] fp32 dQ accumulator, box {32, 1, 128}
+// (128-byte rows), 128B swizzle: the target of the backward's bulk reduce-add.
+bool make_map_f32(CUtensorMap* m, const void* base, int T, int H, int d) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
+    cuuint32_t box[3] = {32, 1, (cuuint32_t)kTile};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct Shape {
     int B, Hq, Hkv, N, T, d;
     bool varlen;
@@ -227,7 +242,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout, 
     BwdParams p;
     std::memset(&p, 0, sizeof(p));
     if (!make_map(&p.tm_q, q, s.T, Hq, d) || !make_map(&p.tm_k, k, s.T, Hkv, d) ||
-        !make_map(&p.tm_v, v, s.T, Hkv, d) || !make_map(&p.tm_do, dout, s.T, Hq, d))
+        !make_map(&p.tm_v, v, s.T, Hkv, d) || !make_map(&p.tm_do, dout, s.T, Hq, d) ||
+        !make_map_f32(&p.tm_dq_acc, static_cast<char*>(workspace) + lay.dq_acc, s.T, Hq, d))
         return FA_ERR_CUDA;
     p.lse = lse;
     p.D = D;

@@ -28,8 +28,11 @@
 //                written bf16 to TMEM (A operand of dV); dS^T = P^T (dP^T - D)
 //                written bf16 to shared memory (A operand of dK, K-major, and
 //                of dQ, read as MN-major)
-//   warps 8..11  dQ drain (one thread per query row; atomic or ordered adds)
-//                and the dK/dV epilogue (one thread per key row)
+//   warps 8..11  dQ drain (one thread per query row): whole tiles are staged
+//                through the dS buffer and merged with bulk tensor reduce-adds,
+//                ragged tiles with per-row vector reductions; ordered by the
+//                semaphores in deterministic mode.  Then the dK/dV epilogue (one
+//                thread per key row)
 // TMEM: S^T [0,128) with P^T over [0,64); dP^T [128,256); dK [256,256+d);
 // dV [256+d, 256+2d); dQ reuses dP^T's columns for d = 128 and has its own
 // columns [384,448) for d = 64.
@@ -65,8 +68,8 @@ struct BwdSmem {
     alignas(1024) uint8_t q[2][BwdCfg<D>::kTileBytes];
     alignas(1024) uint8_t dout[2][BwdCfg<D>::kTileBytes];
     alignas(1024) uint8_t ds[kTile * kTile * 2];  // dS^T: 128 key rows x 128 query cols
-    float lse2[2][kTile];                          // LSE * log2(e) of the stage's query rows
-    float dd[2][kTile];                            // D of the stage's query rows
+    alignas(16) float lse2[2][kTile];              // LSE * log2(e) of the stage's query rows
+    alignas(16) float dd[2][kTile];                // D of the stage's query rows
     alignas(8) uint64_t sched_full[2], sched_empty[2];
     uint64_t kv_full, kv_empty;
     uint64_t qdo_full[2], qdo_empty[2];
@@ -379,7 +382,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_ss(tmem + Cfg::kColDQ, make_sdesc(dsaddr + kk * 2048, 16384, 1024),
                                make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ, kk > 0);
                     mma_commit(smem_u32(&sm.dq_full));
-                    mma_commit(smem_u32(&sm.ds_free));
                     mma_commit(smem_u32(&sm.qdo_empty[st]));
                     ++cnt;
                     ++qit;
@@ -433,17 +435,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tmem_ld32(s_addr + cc * 32, sv);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int x0 = cc * 32 + 2 * e, x1 = x0 + 1;
-                        const float p0 = (x0 >= lo && x0 < hi)
-                                             ? ex2_approx(fmaf(__uint_as_float(sv[2 * e]),
-                                                               p.scale_log2, -l2[x0]))
-                                             : 0.f;
-                        const float p1 = (x1 >= lo && x1 < hi)
-                                             ? ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]),
-                                                               p.scale_log2, -l2[x1]))
-                                             : 0.f;
-                        pk[cc * 16 + e] = pack_bf16x2(p0, p1);
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 lv = reinterpret_cast<const float4*>(l2)[cc * 8 + e4];
+                        const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int e = e4 * 2 + h2;
+                            const int x0 = cc * 32 + 2 * e, x1 = x0 + 1;
+                            const float p0 = (x0 >= lo && x0 < hi)
+                                                 ? ex2_approx(fmaf(__uint_as_float(sv[2 * e]),
+                                                                   p.scale_log2, -la[2 * h2]))
+                                                 : 0.f;
+                            const float p1 = (x1 >= lo && x1 < hi)
+                                                 ? ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]),
+                                                                   p.scale_log2, -la[2 * h2 + 1]))
+                                                 : 0.f;
+                            pk[cc * 16 + e] = pack_bf16x2(p0, p1);
+                        }
                     }
                     uint32_t chunk[16];
 #pragma unroll
@@ -468,13 +476,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tmem_ld_wait();
                     uint32_t out[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int x0 = cc * 32 + 2 * e;
-                        __nv_bfloat162 pp = *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + e]);
-                        const float2 pf = __bfloat1622float2(pp);
-                        const float d0 = pf.x * (__uint_as_float(dv[2 * e]) - dd[x0]);
-                        const float d1 = pf.y * (__uint_as_float(dv[2 * e + 1]) - dd[x0 + 1]);
-                        out[e] = pack_bf16x2(d0, d1);
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 dvv = reinterpret_cast<const float4*>(dd)[cc * 8 + e4];
+                        const float da[4] = {dvv.x, dvv.y, dvv.z, dvv.w};
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int e = e4 * 2 + h2;
+                            __nv_bfloat162 pp =
+                                *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + e]);
+                            const float2 pf = __bfloat1622float2(pp);
+                            const float d0 = pf.x * (__uint_as_float(dv[2 * e]) - da[2 * h2]);
+                            const float d1 = pf.y * (__uint_as_float(dv[2 * e + 1]) - da[2 * h2 + 1]);
+                            out[e] = pack_bf16x2(d0, d1);
+                        }
                     }
                     // 32 query columns = 4 chunks of 16 bytes in block (cc >> 1)
                     uint8_t* blk = ds_row + (cc >> 1) * 16384;
@@ -499,6 +513,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int rr = q4 * 32 + lane;  // row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const bool leader = (warp == 8 && lane == 0);
+        const uint32_t stage_base = smem_u32(sm.ds);
+        uint8_t* stage_row = sm.ds + rr * 128;  // this thread's row in a 16 KB staging slot
+        const int sw = rr & 7;
         int sched_it = 0, unit_it = 0, cnt = 0;
         bool ok = true;
         while (ok) {
@@ -528,27 +545,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                     sem_ok = named_bar_and(1, 128, sem_ok);
                 }
-                const int qr = i * kTile + rr;
-                const bool valid = qr < x.L && sem_ok;
-                float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D;
+                const int row0 = i * kTile;
+                if (row0 + kTile <= x.L) {
+                    // Whole tile: bulk reduce-add, one 32-column chunk at a time, staged
+                    // 128B-swizzled in the dS buffer (its dK/dQ MMAs have completed).
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v);
-                    tmem_ld_wait();
-                    if (valid) {
-                        float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        const int slot = cc & 1;
+                        if (cc >= 2) {  // the reduce that used this slot has read it
+                            if (leader) bulk_wait_group_read<1>();
+                            named_bar_sync(1, 128);
+                        }
+                        uint32_t v[32];
+                        tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v);
+                        tmem_ld_wait();
+                        uint8_t* row = stage_row + slot * 16384;
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            atomicAdd(d4 + e, make_float4(__uint_as_float(v[4 * e]),
-                                                          __uint_as_float(v[4 * e + 1]),
-                                                          __uint_as_float(v[4 * e + 2]),
-                                                          __uint_as_float(v[4 * e + 3])));
+                            *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) =
+                                make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                        fence_proxy_async_smem();
+                        named_bar_sync(1, 128);
+                        if (leader && sem_ok) {
+                            tma_reduce_add_3d(&p.tm_dq_acc, stage_base + slot * 16384, cc * 32,
+                                              x.h, x.t0 + row0);
+                            bulk_commit_group();
+                        }
+                    }
+                } else {
+                    // Ragged last tile of a sequence: per-row vector reductions, valid rows only.
+                    const int qr = row0 + rr;
+                    const bool valid = qr < x.L && sem_ok;
+                    float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D;
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v);
+                        tmem_ld_wait();
+                        if (valid) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[4 * e]),
+                                           __uint_as_float(v[4 * e + 1]),
+                                           __uint_as_float(v[4 * e + 2]),
+                                           __uint_as_float(v[4 * e + 3]));
+                        }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
+                // Hand the dS buffer back once the bulk reduces have read it; in
+                // deterministic mode wait for them to complete before the release below.
+                if (leader) {
+                    if (p.deterministic) {
+                        bulk_wait_group<0>();
+                        fence_proxy_async_global();
+                    } else {
+                        bulk_wait_group_read<0>();
+                    }
+                    mbar_arrive(smem_u32(&sm.ds_free));
+                }
                 if (p.deterministic) {
                     __threadfence();
                     named_bar_sync(1, 128);

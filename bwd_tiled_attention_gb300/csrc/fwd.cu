@@ -324,13 +324,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tc_fence_after();
                 float s[128];
                 {
-                    uint32_t raw[32];
+                    // all four 32-column loads in flight, one wait
+                    uint32_t r0[32], r1[32], r2[32], r3[32];
+                    tmem_ld32(s_addr, r0);
+                    tmem_ld32(s_addr + 32, r1);
+                    tmem_ld32(s_addr + 64, r2);
+                    tmem_ld32(s_addr + 96, r3);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        tmem_ld32(s_addr + c * 32, raw);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[i]);
+                    for (int i = 0; i < 32; ++i) {
+                        s[i] = __uint_as_float(r0[i]);
+                        s[32 + i] = __uint_as_float(r1[i]);
+                        s[64 + i] = __uint_as_float(r2[i]);
+                        s[96 + i] = __uint_as_float(r3[i]);
                     }
                 }
                 const int thr = limit - j * kTile;
@@ -339,9 +345,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int i = 0; i < 128; ++i)
                         if (i >= thr) s[i] = -INFINITY;
                 }
-                float mx = s[0];
+                // row max as an 8-way tree (short dependency chains)
+                float m8[8];
 #pragma unroll
-                for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+                for (int k = 0; k < 8; ++k) m8[k] = s[k];
+#pragma unroll
+                for (int i = 8; i < 128; ++i) m8[i & 7] = fmaxf(m8[i & 7], s[i]);
+                float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 mx *= p.scale_log2;
                 float alpha = 1.f;
                 bool need = false;
@@ -354,6 +365,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     l *= alpha;
                 }
                 const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in 4 independent chains
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
@@ -361,11 +373,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int i = 0; i < 16; ++i) {
                         const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], p.scale_log2, neg));
                         const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], p.scale_log2, neg));
-                        l += p0 + p1;
+                        l4[i & 3] += p0 + p1;
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     tmem_st16(s_addr + c * 16, pk);
                 }
+                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
                 if (__any_sync(0xffffffffu, need)) {
                     // O~ is stable here: S_t(j) was committed after O_t += P_t V of j-1.
 #pragma unroll 1

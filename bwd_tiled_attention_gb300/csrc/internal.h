@@ -24,6 +24,7 @@ struct FwdParams {
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    CUtensorMap tm_dq_acc;         // fp32 map over the dQ accumulator, box {32, 1, 128}
     const float* lse;
     const float* D;
     void* dk;                      // final dK (MHA) -- bf16 or fp32
