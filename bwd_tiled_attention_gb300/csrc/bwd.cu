@@ -218,10 +218,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     const int n_units = hdr->n_units;
+    // Registers: the launch gives every thread 168 (384 x 168 = 64512).  The
+    // producer/MMA warpgroup (warps 0..3) needs few, so each of its warps gives
+    // back to 88 at the top of its role, and the two math warpgroups take 208
+    // each: 128*88 + 256*208 = 64512 exactly.
+    static_assert(128 * 88 + 256 * 208 == 384 * 168, "register split must match the launch");
     const int n_qtiles = hdr->n_qtiles;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        setmaxnreg_dec<88>();
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_k);
@@ -303,6 +309,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        setmaxnreg_dec<88>();
         if (lane == 0) {
             constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
             constexpr uint32_t idKV = make_idesc_bf16(128, D, false, true);
@@ -339,31 +346,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                make_sdesc(qaddr + off, 16, 1024), idS, kk > 0);
                     }
                     mma_commit(smem_u32(&sm.s_full));
-                    // dP^T = V_j dO_i^T  (for d = 128 the dQ drain of the previous step shares columns)
-                    if (Cfg::kDqAliasesDp && cnt > 0 &&
-                        !(ok = wait_or_abort(smem_u32(&sm.dq_free), (cnt - 1) & 1, abort_flag, hdr)))
-                        break;
-                    tc_fence_after();
+                    // dP^T = V_j dO_i^T and dV_j += P^T dO_i, in whichever order their
+                    // inputs become ready (dP first when both are: it is on the critical
+                    // path dQ drain -> dP -> dS -> dK/dQ).  For d = 128, dP reuses the
+                    // TMEM columns the previous step's dQ drain reads; dV reads P^T from
+                    // TMEM and, on a unit's first step, needs the previous unit's dK/dV
+                    // epilogue finished.
+                    {
+                        bool dp_done = false, dv_done = false;
+                        const uint64_t t_start = globaltimer();
+                        while (!(dp_done && dv_done)) {
+                            if (!dp_done &&
+                                (!Cfg::kDqAliasesDp || cnt == 0 ||
+                                 mbar_try_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
+                                tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tmem + Cfg::kColDP, make_sdesc(vaddr + off, 16, 1024),
-                               make_sdesc(doaddr + off, 16, 1024), idS, kk > 0);
+                                for (int kk = 0; kk < D / 16; ++kk) {
+                                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                    mma_ss(tmem + Cfg::kColDP, make_sdesc(vaddr + off, 16, 1024),
+                                           make_sdesc(doaddr + off, 16, 1024), idS, kk > 0);
+                                }
+                                mma_commit(smem_u32(&sm.dp_full));
+                                dp_done = true;
+                                continue;
+                            }
+                            if (!dv_done && mbar_try_wait(smem_u32(&sm.p_ready), cnt & 1) &&
+                                (s != 0 || unit_it == 0 ||
+                                 mbar_try_wait(smem_u32(&sm.dkv_free), (unit_it - 1) & 1))) {
+                                tc_fence_after();
+#pragma unroll
+                                for (int kk = 0; kk < kTile / 16; ++kk)
+                                    mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + kk * 8,
+                                           make_sdesc(doaddr + kk * 2048, 16384, 1024), idKV,
+                                           (s > 0 || kk > 0) ? 1u : 0u);
+                                mma_commit(smem_u32(&sm.s_free));
+                                dv_done = true;
+                                continue;
+                            }
+                            if (*abort_flag || globaltimer() - t_start > kSpinLimitNs) {
+                                raise_abort(abort_flag, hdr, kErrTimeout);
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) break;
                     }
-                    mma_commit(smem_u32(&sm.dp_full));
-                    // dV_j += P^T dO_i  (A = P^T from TMEM)
-                    if (!(ok = wait_or_abort(smem_u32(&sm.p_ready), cnt & 1, abort_flag, hdr))) break;
-                    if (s == 0 && unit_it > 0 &&
-                        !(ok = wait_or_abort(smem_u32(&sm.dkv_free), (unit_it - 1) & 1, abort_flag,
-                                             hdr)))
-                        break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + kk * 8,
-                               make_sdesc(doaddr + kk * 2048, 16384, 1024), idKV,
-                               (s > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(smem_u32(&sm.s_free));
                     // dK_j += dS^T Q_i ; dQ_i = dS K_j  (A = dS^T in shared memory)
                     if (!(ok = wait_or_abort(smem_u32(&sm.ds_ready), cnt & 1, abort_flag, hdr))) break;
                     tc_fence_after();
@@ -396,6 +423,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ compute: P^T and dS^T
+        setmaxnreg_inc<208>();
         const int q4 = warp & 3;
         const int rk = q4 * 32 + lane;                    // key row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -509,6 +537,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+        setmaxnreg_inc<208>();
         const int q4 = warp & 3;
         const int rr = q4 * 32 + lane;  // row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -546,24 +575,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     sem_ok = named_bar_and(1, 128, sem_ok);
                 }
                 const int row0 = i * kTile;
+                // The whole dQ row into registers first, then give the TMEM
+                // columns back at once: the next dP MMA is waiting for them.
+                uint32_t v[D / 32][32];
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc)
+                    tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v[cc]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
                 if (row0 + kTile <= x.L) {
                     // Whole tile: bulk reduce-add, one 32-column chunk at a time, staged
                     // 128B-swizzled in the dS buffer (its dK/dQ MMAs have completed).
-#pragma unroll 1
+#pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc) {
                         const int slot = cc & 1;
                         if (cc >= 2) {  // the reduce that used this slot has read it
                             if (leader) bulk_wait_group_read<1>();
                             named_bar_sync(1, 128);
                         }
-                        uint32_t v[32];
-                        tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v);
-                        tmem_ld_wait();
                         uint8_t* row = stage_row + slot * 16384;
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) =
-                                make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                            *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) = make_uint4(
+                                v[cc][4 * e], v[cc][4 * e + 1], v[cc][4 * e + 2], v[cc][4 * e + 3]);
                         fence_proxy_async_smem();
                         named_bar_sync(1, 128);
                         if (leader && sem_ok) {
@@ -575,26 +611,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 } else {
                     // Ragged last tile of a sequence: per-row vector reductions, valid rows only.
                     const int qr = row0 + rr;
-                    const bool valid = qr < x.L && sem_ok;
-                    float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D;
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v);
-                        tmem_ld_wait();
-                        if (valid) {
+                    if (qr < x.L && sem_ok) {
+                        float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D;
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc)
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[4 * e]),
-                                           __uint_as_float(v[4 * e + 1]),
-                                           __uint_as_float(v[4 * e + 2]),
-                                           __uint_as_float(v[4 * e + 3]));
-                        }
+                                red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[cc][4 * e]),
+                                           __uint_as_float(v[cc][4 * e + 1]),
+                                           __uint_as_float(v[cc][4 * e + 2]),
+                                           __uint_as_float(v[cc][4 * e + 3]));
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
                 // Hand the dS buffer back once the bulk reduces have read it; in
                 // deterministic mode wait for them to complete before the release below.
                 if (leader) {
@@ -674,6 +702,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sm.dkv_free));
             ++unit_it;
         }
+    } else {
+        setmaxnreg_dec<88>();  // warps 2 and 3: TMEM allocation only
     }
 
     tc_fence_before();

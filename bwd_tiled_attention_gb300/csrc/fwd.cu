@@ -80,6 +80,7 @@ __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
     x.g = (int)(((long long)x.h * p.Hkv) / p.Hq);
     seq_bounds(p.cu_seqlens, p.N, x.b, x.t0, x.L);
     const int r0 = x.m * kFwdBlockRows;
+#pragma unroll
     for (int t = 0; t < 2; ++t) {
         const int rs = r0 + t * kTile;  // first row of tile t
         if (rs >= x.L) {
@@ -157,9 +158,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     const int n_units = hdr->n_units;
+    // Registers: the launch gives every thread 168 (384 x 168 = 64512).  The
+    // producer/MMA warpgroup (warps 0..3) needs few, so each of its warps gives
+    // back to 72 at the top of its role, and the two math warpgroups take 216
+    // each: 128*72 + 256*216 = 64512 exactly.
+    static_assert(128 * 72 + 256 * 216 == 384 * 168, "register split must match the launch");
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        setmaxnreg_dec<72>();
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_k);
@@ -183,6 +190,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     break;
                 const uint32_t qbar = smem_u32(&sm.q_full);
                 mbar_arrive_expect_tx(qbar, (x.n[1] > 0 ? 2 : 1) * Cfg::kTileBytes);
+#pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (x.n[t] == 0) continue;
                     for (int c = 0; c < Cfg::kBoxes; ++c)
@@ -219,6 +227,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        setmaxnreg_dec<72>();
         if (lane == 0) {
             constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
             constexpr uint32_t idPV = make_idesc_bf16(128, D, false, true);
@@ -241,7 +250,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 for (int j = 0; j < x.nkv && ok; ++j) {
                     const int st = kv_it % S, par = (kv_it / S) & 1;
                     if (!(ok = wait_or_abort(smem_u32(&sm.k_full[st]), par, abort_flag, hdr))) break;
-                    for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (!ok) break;
                         if (j >= x.n[t]) continue;
                         // S_t / P_t region is free once the previous O_t += P_t V is done
                         if (it[t] > 0 &&
@@ -262,7 +273,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     // the unit's last S MMAs are issued: Q may be overwritten once they finish
                     if (j == x.nkv - 1) mma_commit(smem_u32(&sm.q_empty));
                     if (!(ok = wait_or_abort(smem_u32(&sm.v_full[st]), par, abort_flag, hdr))) break;
-                    for (int t = 0; t < 2 && ok; ++t) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (!ok) break;
                         if (j >= x.n[t]) continue;
                         if (!(ok = wait_or_abort(smem_u32(&sm.p_full[t]), it[t] & 1, abort_flag,
                                                  hdr)))
@@ -287,6 +300,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
                 if (!ok) break;
                 ++unit_it;
+#pragma unroll
                 for (int t = 0; t < 2; ++t) ep[t] += x.n[t] > 0;
             }
             // all issued MMAs complete before TMEM is released
@@ -295,6 +309,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax warpgroups
+        setmaxnreg_inc<216>();
         const int t = (warp - 4) >> 2;          // query tile of this warpgroup
         const int q4 = warp & 3;                // TMEM lane quarter
         const int row = q4 * 32 + lane;         // row within the tile
@@ -314,7 +329,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ++sched_it;
             if (unit.x < 0) break;
             const UnitGeom x = decode_unit(unit, p);
-            const int nt = x.n[t];
+            const int nt = t == 0 ? x.n[0] : x.n[1];
             if (nt == 0) continue;
             const int r = x.m * kFwdBlockRows + t * kTile + row;  // row within the sequence
             const int limit = p.causal ? min(r + 1, x.L) : x.L;   // visible keys: col < limit
@@ -445,6 +460,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.o_free[t]));
         }
+    } else {
+        setmaxnreg_dec<72>();  // warps 2 and 3: TMEM allocation only
     }
 
     tc_fence_before();

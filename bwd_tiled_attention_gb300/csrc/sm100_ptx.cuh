@@ -262,6 +262,20 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- register rebalancing
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same one).  The increases may only draw on what the decreases release from
+// the block's launch allocation.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- misc math
 
 // Hardware base-2 exponential (MUFU), flush-to-zero.
