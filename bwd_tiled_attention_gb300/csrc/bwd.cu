@@ -20,16 +20,21 @@
 // mode, and heaviest-first otherwise.
 //
 // Roles (384 threads):
-//   warp 0       producer: K_j, V_j once per unit, then Q_i, dO_i (TMA) and
-//                LSE_i, D_i (plain loads) through a 2-stage ring
-//   warp 1       MMA issuer (tcgen05, one thread)
+//   warp 0       producer: K_j, V_j once per unit, then Q_i with LSE_i, D_i
+//                (2-stage ring) and dO_i (1 stage) by TMA / plain loads
+//   warp 1       MMA issuer (tcgen05, one thread).  Per step: dP and dV in the
+//                order their inputs arrive, then S of the NEXT step as soon as
+//                dV has released the S columns, then dK and dQ once dS is in
+//                shared memory -- so the compute warps find S(i+1) ready when
+//                they finish dS(i)
 //   warp 2       TMEM allocation
 //   warps 4..7   compute: one thread per key row; P^T = exp2(S^T*c - LSE2),
 //                written bf16 to TMEM (A operand of dV); dS^T = P^T (dP^T - D)
 //                written bf16 to shared memory (A operand of dK, K-major, and
 //                of dQ, read as MN-major)
 //   warps 8..11  dQ drain (one thread per query row): whole tiles are staged
-//                through the dS buffer and merged with bulk tensor reduce-adds,
+//                through a dedicated 32 KB buffer and merged with bulk tensor
+//                reduce-adds,
 //                ragged tiles with per-row vector reductions; ordered by the
 //                semaphores in deterministic mode.  Then the dK/dV epilogue (one
 //                thread per key row)
@@ -65,14 +70,15 @@ template <int D>
 struct BwdSmem {
     alignas(1024) uint8_t k[BwdCfg<D>::kTileBytes];
     alignas(1024) uint8_t v[BwdCfg<D>::kTileBytes];
-    alignas(1024) uint8_t q[2][BwdCfg<D>::kTileBytes];
-    alignas(1024) uint8_t dout[2][BwdCfg<D>::kTileBytes];
-    alignas(1024) uint8_t ds[kTile * kTile * 2];  // dS^T: 128 key rows x 128 query cols
-    alignas(16) float lse2[2][kTile];              // LSE * log2(e) of the stage's query rows
-    alignas(16) float dd[2][kTile];                // D of the stage's query rows
+    alignas(1024) uint8_t q[2][BwdCfg<D>::kTileBytes];   // Q ring (2 stages)
+    alignas(1024) uint8_t dout[BwdCfg<D>::kTileBytes];   // dO (1 stage)
+    alignas(1024) uint8_t ds[kTile * kTile * 2];         // dS^T: 128 key rows x 128 query cols
+    alignas(1024) uint8_t stage[2][kTile * 128];         // dQ staging: 2 slots of 128 rows x 128 B
+    alignas(16) float lse2[2][kTile];                    // LSE * log2(e) of the Q stage's rows
+    alignas(16) float dd[2][kTile];                      // D of the Q stage's rows
     alignas(8) uint64_t sched_full[2], sched_empty[2];
     uint64_t kv_full, kv_empty;
-    uint64_t qdo_full[2], qdo_empty[2];
+    uint64_t q_full[2], q_empty[2], do_full, do_empty;
     uint64_t s_full, dp_full, p_ready, ds_ready, s_free, ds_free, dq_full, dq_free;
     uint64_t dkv_full, dkv_free, drain;
     int2 sched[2];
@@ -189,9 +195,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&sm.sched_full[i]), 1);
             mbar_init(smem_u32(&sm.sched_empty[i]), 1 + 8);
-            mbar_init(smem_u32(&sm.qdo_full[i]), 1 + 32);
-            mbar_init(smem_u32(&sm.qdo_empty[i]), 1);
+            mbar_init(smem_u32(&sm.q_full[i]), 1 + 32);
+            mbar_init(smem_u32(&sm.q_empty[i]), 1);
         }
+        mbar_init(smem_u32(&sm.do_full), 1);
+        mbar_init(smem_u32(&sm.do_empty), 1);
         mbar_init(smem_u32(&sm.kv_full), 1);
         mbar_init(smem_u32(&sm.kv_empty), 1);
         mbar_init(smem_u32(&sm.s_full), 1);
@@ -218,23 +226,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     const int n_units = hdr->n_units;
+    const int n_qtiles = hdr->n_qtiles;
     // Registers: the launch gives every thread 168 (384 x 168 = 64512).  The
     // producer/MMA warpgroup (warps 0..3) needs few, so each of its warps gives
-    // back to 88 at the top of its role, and the two math warpgroups take 208
-    // each: 128*88 + 256*208 = 64512 exactly.
-    static_assert(128 * 88 + 256 * 208 == 384 * 168, "register split must match the launch");
-    const int n_qtiles = hdr->n_qtiles;
+    // back to 104 at the top of its role, and the two math warpgroups take 200
+    // each: 128*104 + 256*200 = 64512 exactly.
+    static_assert(128 * 104 + 256 * 200 == 384 * 168, "register split must match the launch");
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        setmaxnreg_dec<88>();
+        setmaxnreg_dec<104>();
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
             tma_prefetch_desc(&p.tm_do);
         }
-        int sched_it = 0, unit_it = 0, qit = 0;
+        int sched_it = 0, unit_it = 0, c = 0;
         bool ok = true;
         while (ok) {
             const int slot = sched_it & 1;
@@ -258,29 +266,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) {
                 const uint32_t bar = smem_u32(&sm.kv_full);
                 mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
-                for (int c = 0; c < Cfg::kBoxes; ++c) {
-                    tma_load_3d(smem_u32(sm.k) + c * 16384, &p.tm_k, bar, c * 64, x.g,
+                for (int cb = 0; cb < Cfg::kBoxes; ++cb) {
+                    tma_load_3d(smem_u32(sm.k) + cb * 16384, &p.tm_k, bar, cb * 64, x.g,
                                 x.t0 + x.j * kTile);
-                    tma_load_3d(smem_u32(sm.v) + c * 16384, &p.tm_v, bar, c * 64, x.g,
+                    tma_load_3d(smem_u32(sm.v) + cb * 16384, &p.tm_v, bar, cb * 64, x.g,
                                 x.t0 + x.j * kTile);
                 }
             }
             ++unit_it;
-            for (int s = 0; s < x.ni && ok; ++s) {
+            for (int s = 0; s < x.ni && ok; ++s, ++c) {
                 const int i = walk_tile(x, s);
-                const int st = qit & 1;
-                if (!(ok = lane0_wait(smem_u32(&sm.qdo_empty[st]), ((qit >> 1) & 1) ^ 1,
-                                      abort_flag, hdr)))
+                const int st = c & 1;
+                // Q_i (with its LSE and D rows) into the 2-stage ring
+                if (!(ok = lane0_wait(smem_u32(&sm.q_empty[st]), ((c >> 1) & 1) ^ 1, abort_flag,
+                                      hdr)))
                     break;
-                const uint32_t bar = smem_u32(&sm.qdo_full[st]);
+                const uint32_t qbar = smem_u32(&sm.q_full[st]);
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
-                    for (int c = 0; c < Cfg::kBoxes; ++c) {
-                        tma_load_3d(smem_u32(sm.q[st]) + c * 16384, &p.tm_q, bar, c * 64, x.h,
+                    mbar_arrive_expect_tx(qbar, Cfg::kTileBytes);
+                    for (int cb = 0; cb < Cfg::kBoxes; ++cb)
+                        tma_load_3d(smem_u32(sm.q[st]) + cb * 16384, &p.tm_q, qbar, cb * 64, x.h,
                                     x.t0 + i * kTile);
-                        tma_load_3d(smem_u32(sm.dout[st]) + c * 16384, &p.tm_do, bar, c * 64, x.h,
-                                    x.t0 + i * kTile);
-                    }
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -295,28 +301,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     sm.lse2[st][rr] = l2;
                     sm.dd[st][rr] = dv;
                 }
-                mbar_arrive(bar);
-                ++qit;
+                mbar_arrive(qbar);
+                // dO_i into its single stage, once dP and dV of the previous step ran
+                if (!(ok = lane0_wait(smem_u32(&sm.do_empty), (c & 1) ^ 1, abort_flag, hdr)))
+                    break;
+                if (lane == 0) {
+                    const uint32_t dbar = smem_u32(&sm.do_full);
+                    mbar_arrive_expect_tx(dbar, Cfg::kTileBytes);
+                    for (int cb = 0; cb < Cfg::kBoxes; ++cb)
+                        tma_load_3d(smem_u32(sm.dout) + cb * 16384, &p.tm_do, dbar, cb * 64, x.h,
+                                    x.t0 + i * kTile);
+                }
             }
         }
         if (lane == 0) {
+            // never leave a TMA write in flight
             const volatile int* z = &sm.zero;
-            for (int e = 0; e < 2 && e < qit; ++e) {
-                const int it = qit - 1 - e;
-                mbar_wait(smem_u32(&sm.qdo_full[it & 1]), (it >> 1) & 1, z);
+            for (int e = 0; e < 2 && e < c; ++e) {
+                const int it = c - 1 - e;
+                mbar_wait(smem_u32(&sm.q_full[it & 1]), (it >> 1) & 1, z);
             }
+            if (c > 0) mbar_wait(smem_u32(&sm.do_full), (c - 1) & 1, z);
             if (unit_it > 0) mbar_wait(smem_u32(&sm.kv_full), (unit_it - 1) & 1, z);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        setmaxnreg_dec<88>();
+        setmaxnreg_dec<104>();
         if (lane == 0) {
             constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
             constexpr uint32_t idKV = make_idesc_bf16(128, D, false, true);
             constexpr uint32_t idDQ = make_idesc_bf16(128, D, true, true);
-            int sched_it = 0, unit_it = 0, qit = 0, cnt = 0;
+            int sched_it = 0, unit_it = 0, cnt = 0;
             bool ok = true;
             const uint32_t kaddr = smem_u32(sm.k), vaddr = smem_u32(sm.v), dsaddr = smem_u32(sm.ds);
+            const uint32_t doaddr = smem_u32(sm.dout);
+            // S^T(c) = K_j Q_c^T into the S columns: needs Q_c loaded and dV(c-1),
+            // the last reader of the previous P^T in those columns, complete.
+            auto issue_s = [&](int c) -> bool {
+                if (!wait_or_abort(smem_u32(&sm.q_full[c & 1]), (c >> 1) & 1, abort_flag, hdr))
+                    return false;
+                if (c > 0 && !wait_or_abort(smem_u32(&sm.s_free), (c - 1) & 1, abort_flag, hdr))
+                    return false;
+                tc_fence_after();
+                const uint32_t qaddr = smem_u32(sm.q[c & 1]);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(tmem + Cfg::kColS, make_sdesc(kaddr + off, 16, 1024),
+                           make_sdesc(qaddr + off, 16, 1024), idS, kk > 0);
+                }
+                mma_commit(smem_u32(&sm.s_full));
+                return true;
+            };
             while (ok) {
                 const int slot = sched_it & 1;
                 if (!(ok = wait_or_abort(smem_u32(&sm.sched_full[slot]), (sched_it >> 1) & 1,
@@ -328,29 +364,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (unit.x < 0) break;
                 const BUnit x = decode_bunit(unit, p);
                 if (!(ok = wait_or_abort(smem_u32(&sm.kv_full), unit_it & 1, abort_flag, hdr))) break;
-                for (int s = 0; s < x.ni; ++s) {
-                    const int st = qit & 1;
-                    if (!(ok = wait_or_abort(smem_u32(&sm.qdo_full[st]), (qit >> 1) & 1, abort_flag,
-                                             hdr)))
-                        break;
-                    const uint32_t qaddr = smem_u32(sm.q[st]), doaddr = smem_u32(sm.dout[st]);
-                    // S^T = K_j Q_i^T  (the S region is free once dV of the previous step ran)
-                    if (cnt > 0 && !(ok = wait_or_abort(smem_u32(&sm.s_free), (cnt - 1) & 1,
-                                                        abort_flag, hdr)))
-                        break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tmem + Cfg::kColS, make_sdesc(kaddr + off, 16, 1024),
-                               make_sdesc(qaddr + off, 16, 1024), idS, kk > 0);
-                    }
-                    mma_commit(smem_u32(&sm.s_full));
-                    // dP^T = V_j dO_i^T and dV_j += P^T dO_i, in whichever order their
-                    // inputs become ready (dP first when both are: it is on the critical
-                    // path dQ drain -> dP -> dS -> dK/dQ).  For d = 128, dP reuses the
-                    // TMEM columns the previous step's dQ drain reads; dV reads P^T from
-                    // TMEM and, on a unit's first step, needs the previous unit's dK/dV
+                if (!(ok = issue_s(cnt))) break;
+                for (int s = 0; s < x.ni; ++s, ++cnt) {
+                    const int st = cnt & 1;
+                    const uint32_t qaddr = smem_u32(sm.q[st]);
+                    if (!(ok = wait_or_abort(smem_u32(&sm.do_full), cnt & 1, abort_flag, hdr))) break;
+                    // dP^T = V_j dO^T and dV_j += P^T dO in whichever order their inputs
+                    // become ready (dP first when both are: it is on the critical path
+                    // dQ drain -> dP -> dS -> dK/dQ).  For d = 128, dP reuses the TMEM
+                    // columns the previous step's dQ drain reads; dV reads P^T from TMEM
+                    // and, on a unit's first step, needs the previous unit's dK/dV
                     // epilogue finished.
                     {
                         bool dp_done = false, dv_done = false;
@@ -391,7 +414,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                         if (!ok) break;
                     }
-                    // dK_j += dS^T Q_i ; dQ_i = dS K_j  (A = dS^T in shared memory)
+                    mma_commit(smem_u32(&sm.do_empty));  // dO read by dP and dV
+                    // the next step's S, as soon as dV has finished with the S columns
+                    if (s + 1 < x.ni && !(ok = issue_s(cnt + 1))) break;
+                    // dK_j += dS^T Q ; dQ = dS K_j  (A = dS^T in shared memory)
                     if (!(ok = wait_or_abort(smem_u32(&sm.ds_ready), cnt & 1, abort_flag, hdr))) break;
                     tc_fence_after();
 #pragma unroll
@@ -409,9 +435,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_ss(tmem + Cfg::kColDQ, make_sdesc(dsaddr + kk * 2048, 16384, 1024),
                                make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ, kk > 0);
                     mma_commit(smem_u32(&sm.dq_full));
-                    mma_commit(smem_u32(&sm.qdo_empty[st]));
-                    ++cnt;
-                    ++qit;
+                    mma_commit(smem_u32(&sm.ds_free));
+                    mma_commit(smem_u32(&sm.q_empty[st]));
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&sm.dkv_full));
@@ -423,7 +448,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ compute: P^T and dS^T
-        setmaxnreg_inc<208>();
+        setmaxnreg_inc<200>();
         const int q4 = warp & 3;
         const int rk = q4 * 32 + lane;                    // key row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -431,7 +456,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t dp_addr = tmem + lane_off + Cfg::kColDP;
         uint8_t* ds_row = sm.ds + rk * 128;
         const int sw = rk & 7;
-        int sched_it = 0, qit = 0, cnt = 0;
+        int sched_it = 0, cnt = 0;
         bool ok = true;
         while (ok) {
             const int slot = sched_it & 1;
@@ -445,46 +470,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (unit.x < 0) break;
             const BUnit x = decode_bunit(unit, p);
             const int c = x.j * kTile + rk;  // key position within the sequence
-            for (int s = 0; s < x.ni; ++s) {
+            for (int s = 0; s < x.ni; ++s, ++cnt) {
                 const int i = walk_tile(x, s);
-                const int st = qit & 1;
+                const int st = cnt & 1;
                 // visible query columns of this key row: [lo, hi)
                 const int lo = p.causal ? max(0, c - i * kTile) : 0;
                 const int hi = c < x.L ? min(kTile, x.L - i * kTile) : 0;
-                if (!(ok = warp_wait(smem_u32(&sm.qdo_full[st]), (qit >> 1) & 1, abort_flag, hdr)))
+                if (!(ok = warp_wait(smem_u32(&sm.q_full[st]), (cnt >> 1) & 1, abort_flag, hdr)))
                     break;
                 if (!(ok = warp_wait(smem_u32(&sm.s_full), cnt & 1, abort_flag, hdr))) break;
                 tc_fence_after();
                 const float* l2 = sm.lse2[st];
                 uint32_t pk[64];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t sv[32];
-                    tmem_ld32(s_addr + cc * 32, sv);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sv[2][32];  // two 32-column loads in flight, one wait
+                    tmem_ld32(s_addr + half * 64, sv[0]);
+                    tmem_ld32(s_addr + half * 64 + 32, sv[1]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 lv = reinterpret_cast<const float4*>(l2)[cc * 8 + e4];
-                        const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+                    for (int h = 0; h < 2; ++h) {
+                        const int cc = half * 2 + h;
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const int e = e4 * 2 + h2;
-                            const int x0 = cc * 32 + 2 * e, x1 = x0 + 1;
-                            const float p0 = (x0 >= lo && x0 < hi)
-                                                 ? ex2_approx(fmaf(__uint_as_float(sv[2 * e]),
-                                                                   p.scale_log2, -la[2 * h2]))
-                                                 : 0.f;
-                            const float p1 = (x1 >= lo && x1 < hi)
-                                                 ? ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]),
-                                                                   p.scale_log2, -la[2 * h2 + 1]))
-                                                 : 0.f;
-                            pk[cc * 16 + e] = pack_bf16x2(p0, p1);
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 lv = reinterpret_cast<const float4*>(l2)[cc * 8 + e4];
+                            const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int e = e4 * 2 + h2;
+                                const int x0 = cc * 32 + 2 * e, x1 = x0 + 1;
+                                const float p0 =
+                                    (x0 >= lo && x0 < hi)
+                                        ? ex2_approx(fmaf(__uint_as_float(sv[h][2 * e]),
+                                                          p.scale_log2, -la[2 * h2]))
+                                        : 0.f;
+                                const float p1 =
+                                    (x1 >= lo && x1 < hi)
+                                        ? ex2_approx(fmaf(__uint_as_float(sv[h][2 * e + 1]),
+                                                          p.scale_log2, -la[2 * h2 + 1]))
+                                        : 0.f;
+                                pk[cc * 16 + e] = pack_bf16x2(p0, p1);
+                            }
                         }
-                    }
-                    uint32_t chunk[16];
+                        uint32_t chunk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) chunk[e] = pk[cc * 16 + e];
-                    tmem_st16(s_addr + cc * 16, chunk);
+                        for (int e = 0; e < 16; ++e) chunk[e] = pk[cc * 16 + e];
+                        tmem_st16(s_addr + cc * 16, chunk);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -498,54 +530,60 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 const float* dd = sm.dd[st];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t dv[32];
-                    tmem_ld32(dp_addr + cc * 32, dv);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t dv[2][32];
+                    tmem_ld32(dp_addr + half * 64, dv[0]);
+                    tmem_ld32(dp_addr + half * 64 + 32, dv[1]);
                     tmem_ld_wait();
-                    uint32_t out[16];
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 dvv = reinterpret_cast<const float4*>(dd)[cc * 8 + e4];
-                        const float da[4] = {dvv.x, dvv.y, dvv.z, dvv.w};
+                    for (int h = 0; h < 2; ++h) {
+                        const int cc = half * 2 + h;
+                        uint32_t out[16];
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const int e = e4 * 2 + h2;
-                            __nv_bfloat162 pp =
-                                *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + e]);
-                            const float2 pf = __bfloat1622float2(pp);
-                            const float d0 = pf.x * (__uint_as_float(dv[2 * e]) - da[2 * h2]);
-                            const float d1 = pf.y * (__uint_as_float(dv[2 * e + 1]) - da[2 * h2 + 1]);
-                            out[e] = pack_bf16x2(d0, d1);
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 dvv = reinterpret_cast<const float4*>(dd)[cc * 8 + e4];
+                            const float da[4] = {dvv.x, dvv.y, dvv.z, dvv.w};
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int e = e4 * 2 + h2;
+                                __nv_bfloat162 pp =
+                                    *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + e]);
+                                const float2 pf = __bfloat1622float2(pp);
+                                const float d0 =
+                                    pf.x * (__uint_as_float(dv[h][2 * e]) - da[2 * h2]);
+                                const float d1 =
+                                    pf.y * (__uint_as_float(dv[h][2 * e + 1]) - da[2 * h2 + 1]);
+                                out[e] = pack_bf16x2(d0, d1);
+                            }
                         }
-                    }
-                    // 32 query columns = 4 chunks of 16 bytes in block (cc >> 1)
-                    uint8_t* blk = ds_row + (cc >> 1) * 16384;
+                        // 32 query columns = 4 chunks of 16 bytes in block (cc >> 1)
+                        uint8_t* blk = ds_row + (cc >> 1) * 16384;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int ch = (cc & 1) * 4 + e;
-                        *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
-                            make_uint4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e) {
+                            const int ch = (cc & 1) * 4 + e;
+                            *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
+                                make_uint4(out[4 * e], out[4 * e + 1], out[4 * e + 2],
+                                           out[4 * e + 3]);
+                        }
                     }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sm.ds_ready));
-                ++cnt;
-                ++qit;
             }
         }
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dQ drain + dK/dV epilogue
-        setmaxnreg_inc<208>();
+        setmaxnreg_inc<200>();
         const int q4 = warp & 3;
         const int rr = q4 * 32 + lane;  // row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const bool leader = (warp == 8 && lane == 0);
-        const uint32_t stage_base = smem_u32(sm.ds);
-        uint8_t* stage_row = sm.ds + rr * 128;  // this thread's row in a 16 KB staging slot
+        const uint32_t stage_base = smem_u32(sm.stage[0]);
+        uint8_t* stage_row = sm.stage[0] + rr * 128;  // this thread's row in a staging slot
         const int sw = rr & 7;
-        int sched_it = 0, unit_it = 0, cnt = 0;
+        int sched_it = 0, unit_it = 0, cnt = 0, chunk = 0;
         bool ok = true;
         while (ok) {
             const int slot = sched_it & 1;
@@ -586,16 +624,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
                 if (row0 + kTile <= x.L) {
-                    // Whole tile: bulk reduce-add, one 32-column chunk at a time, staged
-                    // 128B-swizzled in the dS buffer (its dK/dQ MMAs have completed).
+                    // Whole tile: bulk reduce-add, one 32-column chunk at a time,
+                    // staged 128B-swizzled through two 16 KB slots.
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        const int slot = cc & 1;
-                        if (cc >= 2) {  // the reduce that used this slot has read it
-                            if (leader) bulk_wait_group_read<1>();
-                            named_bar_sync(1, 128);
-                        }
-                        uint8_t* row = stage_row + slot * 16384;
+                    for (int cc = 0; cc < D / 32; ++cc, ++chunk) {
+                        const int sl = chunk & 1;
+                        // the reduce that last used this slot has read it
+                        if (leader) bulk_wait_group_read<1>();
+                        named_bar_sync(1, 128);
+                        uint8_t* row = stage_row + sl * (kTile * 128);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) = make_uint4(
@@ -603,10 +640,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         fence_proxy_async_smem();
                         named_bar_sync(1, 128);
                         if (leader && sem_ok) {
-                            tma_reduce_add_3d(&p.tm_dq_acc, stage_base + slot * 16384, cc * 32,
-                                              x.h, x.t0 + row0);
-                            bulk_commit_group();
+                            tma_reduce_add_3d(&p.tm_dq_acc, stage_base + sl * (kTile * 128),
+                                              cc * 32, x.h, x.t0 + row0);
                         }
+                        if (leader) bulk_commit_group();
                     }
                 } else {
                     // Ragged last tile of a sequence: per-row vector reductions, valid rows only.
@@ -623,18 +660,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                            __uint_as_float(v[cc][4 * e + 3]));
                     }
                 }
-                // Hand the dS buffer back once the bulk reduces have read it; in
-                // deterministic mode wait for them to complete before the release below.
-                if (leader) {
-                    if (p.deterministic) {
+                if (p.deterministic) {
+                    // this contribution must be complete before the next one may start
+                    if (leader) {
                         bulk_wait_group<0>();
                         fence_proxy_async_global();
-                    } else {
-                        bulk_wait_group_read<0>();
                     }
-                    mbar_arrive(smem_u32(&sm.ds_free));
-                }
-                if (p.deterministic) {
                     __threadfence();
                     named_bar_sync(1, 128);
                     if (leader && sem_ok) red_release_gpu_add(sem, 1);
@@ -702,8 +733,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sm.dkv_free));
             ++unit_it;
         }
+        // the staging slots must not be read after the CTA exits
+        if (leader) bulk_wait_group<0>();
     } else {
-        setmaxnreg_dec<88>();  // warps 2 and 3: TMEM allocation only
+        setmaxnreg_dec<104>();  // warps 2 and 3: TMEM allocation only
     }
 
     tc_fence_before();
