@@ -19,7 +19,7 @@
 // write.  The scheduler launches units with descending j in deterministic
 // mode, and heaviest-first otherwise.
 //
-// Roles (384 threads):
+// Roles (512 threads):
 //   warp 0       producer: K_j, V_j once per unit, then Q_i with LSE_i, D_i
 //                (2-stage ring) and dO_i (1 stage) by TMA / plain loads
 //   warp 1       MMA issuer (tcgen05, one thread).  Per step: dP and dV in the
@@ -28,11 +28,12 @@
 //                shared memory -- so the compute warps find S(i+1) ready when
 //                they finish dS(i)
 //   warp 2       TMEM allocation
-//   warps 4..7   compute: one thread per key row; P^T = exp2(S^T*c - LSE2),
+//   warps 4..11  compute, two warpgroups splitting the 128 query columns of a
+//                step into halves; one thread per (key row, half): P^T = exp2(S^T*c - LSE2),
 //                written bf16 to TMEM (A operand of dV); dS^T = P^T (dP^T - D)
 //                written bf16 to shared memory (A operand of dK, K-major, and
 //                of dQ, read as MN-major)
-//   warps 8..11  dQ drain (one thread per query row): whole tiles are staged
+//   warps 12..15 dQ drain (one thread per query row): whole tiles are staged
 //                through a dedicated 32 KB buffer and merged with bulk tensor
 //                reduce-adds,
 //                ragged tiles with per-row vector reductions; ordered by the
@@ -54,7 +55,7 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -170,6 +171,30 @@ __device__ bool sem_wait(const int* sem, int target, const WsHeader* hdr) {
     }
 }
 
+// P^T for one 32-column chunk of a key row: exp2(S^T * c - LSE2) as packed
+// bf16 pairs; with MASK, columns outside [lo, hi) are zero.
+template <bool MASK>
+__device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* l2, float c2,
+                                        int lo, int hi, int xb, uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 lv = reinterpret_cast<const float4*>(l2)[e4];
+        const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int e = e4 * 2 + h2;
+            float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), c2, -la[2 * h2]));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), c2, -la[2 * h2 + 1]));
+            if (MASK) {
+                const int x0 = xb + 2 * e, x1 = x0 + 1;
+                p0 = (x0 >= lo && x0 < hi) ? p0 : 0.f;
+                p1 = (x1 >= lo && x1 < hi) ? p1 : 0.f;
+            }
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
@@ -194,7 +219,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&sm.sched_full[i]), 1);
-            mbar_init(smem_u32(&sm.sched_empty[i]), 1 + 8);
+            mbar_init(smem_u32(&sm.sched_empty[i]), 1 + 12);
             mbar_init(smem_u32(&sm.q_full[i]), 1 + 32);
             mbar_init(smem_u32(&sm.q_empty[i]), 1);
         }
@@ -204,8 +229,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(smem_u32(&sm.kv_empty), 1);
         mbar_init(smem_u32(&sm.s_full), 1);
         mbar_init(smem_u32(&sm.dp_full), 1);
-        mbar_init(smem_u32(&sm.p_ready), 4);
-        mbar_init(smem_u32(&sm.ds_ready), 4);
+        mbar_init(smem_u32(&sm.p_ready), 8);
+        mbar_init(smem_u32(&sm.ds_ready), 8);
         mbar_init(smem_u32(&sm.s_free), 1);
         mbar_init(smem_u32(&sm.ds_free), 1);
         mbar_init(smem_u32(&sm.dq_full), 1);
@@ -227,15 +252,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tmem = sm.tmem_base;
     const int n_units = hdr->n_units;
     const int n_qtiles = hdr->n_qtiles;
-    // Registers: the launch gives every thread 168 (384 x 168 = 64512).  The
-    // producer/MMA warpgroup (warps 0..3) needs few, so each of its warps gives
-    // back to 104 at the top of its role, and the two math warpgroups take 200
-    // each: 128*104 + 256*200 = 64512 exactly.
-    static_assert(128 * 104 + 256 * 200 == 384 * 168, "register split must match the launch");
+    // Registers: the launch gives every thread 128 (512 x 128 = 65536).  The
+    // producer/MMA warpgroup (warps 0..3) gives back to 80 at the top of each
+    // role, and the three math warpgroups take 144 each:
+    // 128*80 + 384*144 = 65536 exactly.
+    static_assert(128 * 80 + 384 * 144 == kBwdThreads * 128, "register split must match the launch");
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        setmaxnreg_dec<104>();
+        setmaxnreg_dec<80>();
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_k);
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        setmaxnreg_dec<104>();
+        setmaxnreg_dec<80>();
         if (lane == 0) {
             constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
             constexpr uint32_t idKV = make_idesc_bf16(128, D, false, true);
@@ -446,15 +471,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit(smem_u32(&sm.drain));
             mbar_wait(smem_u32(&sm.drain), 0, &sm.zero);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ compute: P^T and dS^T
-        setmaxnreg_inc<200>();
+        setmaxnreg_inc<144>();
         const int q4 = warp & 3;
+        const int hc = (warp - 4) >> 2;                   // query-column half of this warpgroup
         const int rk = q4 * 32 + lane;                    // key row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + Cfg::kColS;
         const uint32_t dp_addr = tmem + lane_off + Cfg::kColDP;
-        uint8_t* ds_row = sm.ds + rk * 128;
+        uint8_t* ds_row = sm.ds + hc * 16384 + rk * 128;  // this half's 64-column block
         const int sw = rk & 7;
         int sched_it = 0, cnt = 0;
         bool ok = true;
@@ -473,49 +499,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int s = 0; s < x.ni; ++s, ++cnt) {
                 const int i = walk_tile(x, s);
                 const int st = cnt & 1;
-                // visible query columns of this key row: [lo, hi)
+                // visible query columns of this key row: [lo, hi); the warp skips the
+                // mask when every row sees every column
                 const int lo = p.causal ? max(0, c - i * kTile) : 0;
                 const int hi = c < x.L ? min(kTile, x.L - i * kTile) : 0;
+                const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kTile);
                 if (!(ok = warp_wait(smem_u32(&sm.q_full[st]), (cnt >> 1) & 1, abort_flag, hdr)))
                     break;
                 if (!(ok = warp_wait(smem_u32(&sm.s_full), cnt & 1, abort_flag, hdr))) break;
                 tc_fence_after();
-                const float* l2 = sm.lse2[st];
-                uint32_t pk[64];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sv[2][32];  // two 32-column loads in flight, one wait
-                    tmem_ld32(s_addr + half * 64, sv[0]);
-                    tmem_ld32(s_addr + half * 64 + 32, sv[1]);
+                const float* l2 = sm.lse2[st] + hc * 64;
+                uint32_t pk[2][16];
+                {
+                    uint32_t sv[2][32];  // this half's two 32-column loads, one wait
+                    tmem_ld32(s_addr + hc * 64, sv[0]);
+                    tmem_ld32(s_addr + hc * 64 + 32, sv[1]);
                     tmem_ld_wait();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int cc = half * 2 + h;
-#pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 lv = reinterpret_cast<const float4*>(l2)[cc * 8 + e4];
-                            const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-                            for (int h2 = 0; h2 < 2; ++h2) {
-                                const int e = e4 * 2 + h2;
-                                const int x0 = cc * 32 + 2 * e, x1 = x0 + 1;
-                                const float p0 =
-                                    (x0 >= lo && x0 < hi)
-                                        ? ex2_approx(fmaf(__uint_as_float(sv[h][2 * e]),
-                                                          p.scale_log2, -la[2 * h2]))
-                                        : 0.f;
-                                const float p1 =
-                                    (x1 >= lo && x1 < hi)
-                                        ? ex2_approx(fmaf(__uint_as_float(sv[h][2 * e + 1]),
-                                                          p.scale_log2, -la[2 * h2 + 1]))
-                                        : 0.f;
-                                pk[cc * 16 + e] = pack_bf16x2(p0, p1);
-                            }
-                        }
-                        uint32_t chunk[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) chunk[e] = pk[cc * 16 + e];
-                        tmem_st16(s_addr + cc * 16, chunk);
+                        const int xb = hc * 64 + h * 32;  // first query column of the chunk
+                        if (full)
+                            p_chunk<false>(sv[h], l2 + h * 32, p.scale_log2, lo, hi, xb, pk[h]);
+                        else
+                            p_chunk<true>(sv[h], l2 + h * 32, p.scale_log2, lo, hi, xb, pk[h]);
+                        tmem_st16(s_addr + (hc * 2 + h) * 16, pk[h]);
                     }
                 }
                 tmem_st_wait();
@@ -528,26 +535,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     !(ok = warp_wait(smem_u32(&sm.ds_free), (cnt - 1) & 1, abort_flag, hdr)))
                     break;
                 tc_fence_after();
-                const float* dd = sm.dd[st];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                const float* dd = sm.dd[st] + hc * 64;
+                {
                     uint32_t dv[2][32];
-                    tmem_ld32(dp_addr + half * 64, dv[0]);
-                    tmem_ld32(dp_addr + half * 64 + 32, dv[1]);
+                    tmem_ld32(dp_addr + hc * 64, dv[0]);
+                    tmem_ld32(dp_addr + hc * 64 + 32, dv[1]);
                     tmem_ld_wait();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int cc = half * 2 + h;
                         uint32_t out[16];
 #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 dvv = reinterpret_cast<const float4*>(dd)[cc * 8 + e4];
+                            const float4 dvv = reinterpret_cast<const float4*>(dd + h * 32)[e4];
                             const float da[4] = {dvv.x, dvv.y, dvv.z, dvv.w};
 #pragma unroll
                             for (int h2 = 0; h2 < 2; ++h2) {
                                 const int e = e4 * 2 + h2;
                                 __nv_bfloat162 pp =
-                                    *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + e]);
+                                    *reinterpret_cast<const __nv_bfloat162*>(&pk[h][e]);
                                 const float2 pf = __bfloat1622float2(pp);
                                 const float d0 =
                                     pf.x * (__uint_as_float(dv[h][2 * e]) - da[2 * h2]);
@@ -556,12 +561,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 out[e] = pack_bf16x2(d0, d1);
                             }
                         }
-                        // 32 query columns = 4 chunks of 16 bytes in block (cc >> 1)
-                        uint8_t* blk = ds_row + (cc >> 1) * 16384;
+                        // 32 query columns = 4 chunks of 16 bytes of this half's block
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int ch = (cc & 1) * 4 + e;
-                            *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
+                            const int ch = h * 4 + e;
+                            *reinterpret_cast<uint4*>(ds_row + ((ch ^ sw) << 4)) =
                                 make_uint4(out[4 * e], out[4 * e + 1], out[4 * e + 2],
                                            out[4 * e + 3]);
                         }
@@ -573,13 +577,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (lane == 0) mbar_arrive(smem_u32(&sm.ds_ready));
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ drain + dK/dV epilogue
-        setmaxnreg_inc<200>();
+        setmaxnreg_inc<144>();
         const int q4 = warp & 3;
         const int rr = q4 * 32 + lane;  // row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const bool leader = (warp == 8 && lane == 0);
+        const bool leader = (warp == 12 && lane == 0);
         const uint32_t stage_base = smem_u32(sm.stage[0]);
         uint8_t* stage_row = sm.stage[0] + rr * 128;  // this thread's row in a staging slot
         const int sw = rr & 7;
@@ -613,51 +617,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     sem_ok = named_bar_and(1, 128, sem_ok);
                 }
                 const int row0 = i * kTile;
-                // The whole dQ row into registers first, then give the TMEM
-                // columns back at once: the next dP MMA is waiting for them.
-                uint32_t v[D / 32][32];
+                // dQ row in halves of 64 columns; the TMEM columns go back as soon as
+                // the last half is in registers (the next dP MMA waits for them).
+                const bool whole = row0 + kTile <= x.L;
+                const int qr = row0 + rr;
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc)
-                    tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v[cc]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
-                if (row0 + kTile <= x.L) {
-                    // Whole tile: bulk reduce-add, one 32-column chunk at a time,
-                    // staged 128B-swizzled through two 16 KB slots.
-#pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc, ++chunk) {
-                        const int sl = chunk & 1;
-                        // the reduce that last used this slot has read it
-                        if (leader) bulk_wait_group_read<1>();
-                        named_bar_sync(1, 128);
-                        uint8_t* row = stage_row + sl * (kTile * 128);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) = make_uint4(
-                                v[cc][4 * e], v[cc][4 * e + 1], v[cc][4 * e + 2], v[cc][4 * e + 3]);
-                        fence_proxy_async_smem();
-                        named_bar_sync(1, 128);
-                        if (leader && sem_ok) {
-                            tma_reduce_add_3d(&p.tm_dq_acc, stage_base + sl * (kTile * 128),
-                                              cc * 32, x.h, x.t0 + row0);
-                        }
-                        if (leader) bulk_commit_group();
+                for (int hf = 0; hf < D / 64; ++hf) {
+                    uint32_t v[2][32];
+                    tmem_ld32(tmem + lane_off + Cfg::kColDQ + hf * 64, v[0]);
+                    tmem_ld32(tmem + lane_off + Cfg::kColDQ + hf * 64 + 32, v[1]);
+                    tmem_ld_wait();
+                    if (hf == D / 64 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
                     }
-                } else {
-                    // Ragged last tile of a sequence: per-row vector reductions, valid rows only.
-                    const int qr = row0 + rr;
-                    if (qr < x.L && sem_ok) {
-                        float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D;
+                    if (whole) {
+                        // Whole tile: bulk reduce-add, one 32-column chunk at a time,
+                        // staged 128B-swizzled through two 16 KB slots.
 #pragma unroll
-                        for (int cc = 0; cc < D / 32; ++cc)
+                        for (int h = 0; h < 2; ++h, ++chunk) {
+                            const int cc = hf * 2 + h;
+                            const int sl = chunk & 1;
+                            // the reduce that last used this slot has read it
+                            if (leader) bulk_wait_group_read<1>();
+                            named_bar_sync(1, 128);
+                            uint8_t* row = stage_row + sl * (kTile * 128);
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[cc][4 * e]),
-                                           __uint_as_float(v[cc][4 * e + 1]),
-                                           __uint_as_float(v[cc][4 * e + 2]),
-                                           __uint_as_float(v[cc][4 * e + 3]));
+                                *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) =
+                                    make_uint4(v[h][4 * e], v[h][4 * e + 1], v[h][4 * e + 2],
+                                               v[h][4 * e + 3]);
+                            fence_proxy_async_smem();
+                            named_bar_sync(1, 128);
+                            if (leader && sem_ok)
+                                tma_reduce_add_3d(&p.tm_dq_acc, stage_base + sl * (kTile * 128),
+                                                  cc * 32, x.h, x.t0 + row0);
+                            if (leader) bulk_commit_group();
+                        }
+                    } else if (qr < x.L && sem_ok) {
+                        // Ragged last tile of a sequence: per-row vector reductions.
+                        float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D + hf * 64;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                red_add_v4(dst + h * 32 + 4 * e, __uint_as_float(v[h][4 * e]),
+                                           __uint_as_float(v[h][4 * e + 1]),
+                                           __uint_as_float(v[h][4 * e + 2]),
+                                           __uint_as_float(v[h][4 * e + 3]));
                     }
                 }
                 if (p.deterministic) {
@@ -736,7 +744,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // the staging slots must not be read after the CTA exits
         if (leader) bulk_wait_group<0>();
     } else {
-        setmaxnreg_dec<104>();  // warps 2 and 3: TMEM allocation only
+        setmaxnreg_dec<80>();  // warps 2 and 3: TMEM allocation only
     }
 
     tc_fence_before();
