@@ -12,12 +12,14 @@
 // memory, either with fp32 atomics or -- deterministic mode, section 3.2 of
 // the same page -- in a fixed order enforced by one semaphore per dQ tile.
 //
-// Walk order (section 3.3.1): unit j visits query tiles i = j, j+1, ...
-// (wrapping around for non-causal attention), so the contribution of unit j
-// to dQ tile i is the ((i - j) mod n)-th one, contributions to a tile arrive
-// in descending j, and under the causal mask no unit waits on its first dQ
-// write.  The scheduler launches units with descending j in deterministic
-// mode, and heaviest-first otherwise.
+// Walk order (section 3.3.1): in deterministic mode unit j visits query tiles
+// i = j, j+1, ... (wrapping around for non-causal attention), so the
+// contribution of unit j to dQ tile i is the ((i - j) mod n)-th one,
+// contributions to a tile arrive in descending j, and under the causal mask no
+// unit waits on its first dQ write; the scheduler launches units with
+// descending j.  In atomic mode all units of a (sequence, head) walk the query
+// tiles in one common order (for L2 reuse of Q, dO and the dQ accumulator) and
+// are launched heaviest-first.
 //
 // Roles (512 threads):
 //   warp 0       producer: K_j, V_j once per unit, then Q_i with LSE_i, D_i
@@ -106,9 +108,19 @@ __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
 }
 
 // Query tile visited at step s of unit x.
-__device__ __forceinline__ int walk_tile(const BUnit& x, int s) {
-    int i = x.j + s;
-    return i >= x.nt ? i - x.nt : i;
+//  - deterministic mode: i = j, j+1, ... (wrapping for non-causal), so unit j's
+//    contribution to tile i is the ((i - j) mod n)-th and no unit waits on its
+//    first dQ write;
+//  - atomic mode: every unit of a (sequence, head) walks the tiles in the same
+//    order -- descending from the last tile under the causal mask, ascending
+//    otherwise -- so units running side by side load the same Q/dO tile and
+//    reduce into the same dQ tile while it is resident in L2.
+__device__ __forceinline__ int walk_tile(const BUnit& x, int s, int deterministic, int causal) {
+    if (deterministic) {
+        const int i = x.j + s;
+        return i >= x.nt ? i - x.nt : i;
+    }
+    return causal ? x.nt - 1 - s : s;
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* flag, WsHeader* hdr, int code) {
@@ -300,7 +312,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             ++unit_it;
             for (int s = 0; s < x.ni && ok; ++s, ++c) {
-                const int i = walk_tile(x, s);
+                const int i = walk_tile(x, s, p.deterministic, p.causal);
                 const int st = c & 1;
                 // Q_i (with its LSE and D rows) into the 2-stage ring
                 if (!(ok = lane0_wait(smem_u32(&sm.q_empty[st]), ((c >> 1) & 1) ^ 1, abort_flag,
@@ -440,25 +452,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (!ok) break;
                     }
                     mma_commit(smem_u32(&sm.do_empty));  // dO read by dP and dV
-                    // the next step's S, as soon as dV has finished with the S columns
-                    if (s + 1 < x.ni && !(ok = issue_s(cnt + 1))) break;
-                    // dK_j += dS^T Q ; dQ = dS K_j  (A = dS^T in shared memory)
-                    if (!(ok = wait_or_abort(smem_u32(&sm.ds_ready), cnt & 1, abort_flag, hdr))) break;
-                    tc_fence_after();
+                    // Then the next step's S (needs Q(c+1) and dV(c) done with the S
+                    // columns) and this step's dK/dQ (need dS in shared memory), in
+                    // whichever order their inputs arrive; S first when both are, since
+                    // the compute warps start the next step with it.
+                    {
+                        bool s_done = s + 1 >= x.ni, k_done = false;
+                        const uint64_t t_start = globaltimer();
+                        while (!(s_done && k_done)) {
+                            if (!s_done &&
+                                mbar_try_wait(smem_u32(&sm.q_full[(cnt + 1) & 1]),
+                                              ((cnt + 1) >> 1) & 1) &&
+                                mbar_try_wait(smem_u32(&sm.s_free), cnt & 1)) {
+                                tc_fence_after();
+                                const uint32_t qn = smem_u32(sm.q[(cnt + 1) & 1]);
 #pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tmem + Cfg::kColDK, make_sdesc(dsaddr + off, 16, 1024),
-                               make_sdesc(qaddr + kk * 2048, 16384, 1024), idKV,
-                               (s > 0 || kk > 0) ? 1u : 0u);
+                                for (int kk = 0; kk < D / 16; ++kk) {
+                                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                    mma_ss(tmem + Cfg::kColS, make_sdesc(kaddr + off, 16, 1024),
+                                           make_sdesc(qn + off, 16, 1024), idS, kk > 0);
+                                }
+                                mma_commit(smem_u32(&sm.s_full));
+                                s_done = true;
+                                continue;
+                            }
+                            if (!k_done && mbar_try_wait(smem_u32(&sm.ds_ready), cnt & 1) &&
+                                (Cfg::kDqAliasesDp || cnt == 0 ||
+                                 mbar_try_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
+                                tc_fence_after();
+                                // dK_j += dS^T Q ; dQ = dS K_j  (A = dS^T in shared memory)
+#pragma unroll
+                                for (int kk = 0; kk < kTile / 16; ++kk) {
+                                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                    mma_ss(tmem + Cfg::kColDK, make_sdesc(dsaddr + off, 16, 1024),
+                                           make_sdesc(qaddr + kk * 2048, 16384, 1024), idKV,
+                                           (s > 0 || kk > 0) ? 1u : 0u);
+                                }
+#pragma unroll
+                                for (int kk = 0; kk < kTile / 16; ++kk)
+                                    mma_ss(tmem + Cfg::kColDQ,
+                                           make_sdesc(dsaddr + kk * 2048, 16384, 1024),
+                                           make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ,
+                                           kk > 0);
+                                k_done = true;
+                                continue;
+                            }
+                            if (*abort_flag || globaltimer() - t_start > kSpinLimitNs) {
+                                raise_abort(abort_flag, hdr, kErrTimeout);
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) break;
                     }
-                    if (!Cfg::kDqAliasesDp && cnt > 0 &&
-                        !(ok = wait_or_abort(smem_u32(&sm.dq_free), (cnt - 1) & 1, abort_flag, hdr)))
-                        break;
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColDQ, make_sdesc(dsaddr + kk * 2048, 16384, 1024),
-                               make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ, kk > 0);
                     mma_commit(smem_u32(&sm.dq_full));
                     mma_commit(smem_u32(&sm.ds_free));
                     mma_commit(smem_u32(&sm.q_empty[st]));
@@ -497,7 +543,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const BUnit x = decode_bunit(unit, p);
             const int c = x.j * kTile + rk;  // key position within the sequence
             for (int s = 0; s < x.ni; ++s, ++cnt) {
-                const int i = walk_tile(x, s);
+                const int i = walk_tile(x, s, p.deterministic, p.causal);
                 const int st = cnt & 1;
                 // visible query columns of this key row: [lo, hi); the warp skips the
                 // mask when every row sees every column
@@ -601,7 +647,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (unit.x < 0) break;
             const BUnit x = decode_bunit(unit, p);
             for (int s = 0; s < x.ni; ++s) {
-                const int i = walk_tile(x, s);
+                const int i = walk_tile(x, s, p.deterministic, p.causal);
                 if (!(ok = wg_wait(smem_u32(&sm.dq_full), cnt & 1, abort_flag, hdr))) break;
                 tc_fence_after();
                 int* sem = nullptr;
