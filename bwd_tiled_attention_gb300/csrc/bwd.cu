@@ -41,7 +41,8 @@
 //                ragged tiles with per-row vector reductions; ordered by the
 //                semaphores in deterministic mode.  Then the dK/dV epilogue (one
 //                thread per key row)
-// TMEM: S^T [0,128) with P^T over [0,64); dP^T [128,256); dK [256,256+d);
+// TMEM: S^T [0,128), with the bf16 P^T of each 64-column half packed over the
+// first 32 columns of that half ([0,32) and [64,96)); dP^T [128,256); dK [256,256+d);
 // dV [256+d, 256+2d); dQ reuses dP^T's columns for d = 128 and has its own
 // columns [384,448) for d = 64.
 #include <cuda.h>
@@ -434,9 +435,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 (s != 0 || unit_it == 0 ||
                                  mbar_try_wait(smem_u32(&sm.dkv_free), (unit_it - 1) & 1))) {
                                 tc_fence_after();
+                                // P^T of query columns [64h, 64h+64) sits in TMEM
+                                // columns [64h, 64h+32)
 #pragma unroll
                                 for (int kk = 0; kk < kTile / 16; ++kk)
-                                    mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + kk * 8,
+                                    mma_ts(tmem + Cfg::kColDV,
+                                           tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                                            make_sdesc(doaddr + kk * 2048, 16384, 1024), idKV,
                                            (s > 0 || kk > 0) ? 1u : 0u);
                                 mma_commit(smem_u32(&sm.s_free));
@@ -568,7 +572,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             p_chunk<false>(sv[h], l2 + h * 32, p.scale_log2, lo, hi, xb, pk[h]);
                         else
                             p_chunk<true>(sv[h], l2 + h * 32, p.scale_log2, lo, hi, xb, pk[h]);
-                        tmem_st16(s_addr + (hc * 2 + h) * 16, pk[h]);
+                        // into this half's own S^T columns, which this warp has
+                        // already read (the other half's are still being read)
+                        tmem_st16(s_addr + hc * 64 + h * 16, pk[h]);
                     }
                 }
                 tmem_st_wait();
@@ -801,43 +807,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
-// D = rowsum(dO * O) per (token, head); zero the dQ accumulator row and the semaphores.
+// D = rowsum(dO * O) per (token, head); zero the dQ accumulator row and the
+// semaphores.  Each lane takes 8 elements (16-byte loads), D/8 lanes per row,
+// so a warp covers 32/(D/8) rows per pass.
 template <int D, bool O_FP32>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const void* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                           float* __restrict__ Dout, float* __restrict__ dq_acc,
                           int* __restrict__ sems, long long n_sems, int T, int Hq) {
+    constexpr int LPR = D / 8;     // lanes per row
+    constexpr int RPW = 32 / LPR;  // rows per warp pass
     const long long rows = (long long)T * Hq;
     const long long warp_g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr int E = D / 32;  // elements per lane
-    for (long long r = warp_g; r < rows; r += nwarps) {
-        const long long t = r / Hq, h = r % Hq;
-        const size_t base = (size_t)r * D + lane * E;
+    const int sub = lane / LPR, l = lane % LPR;
+    for (long long r0 = warp_g * RPW; r0 < rows; r0 += nwarps * RPW) {
+        const long long r = r0 + sub;
+        const bool valid = r < rows;
         float acc = 0.f;
-        float ov[E], dv[E];
-        if (O_FP32) {
-            const float* op = static_cast<const float*>(o) + base;
+        if (valid) {
+            const size_t base = (size_t)r * D + (size_t)l * 8;
+            const uint4 dv = *reinterpret_cast<const uint4*>(dout + base);
+            const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+            float ov[8];
+            if (O_FP32) {
+                const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base);
+                const float4 b =
+                    *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base + 4);
+                ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w;
+                ov[4] = b.x; ov[5] = b.y; ov[6] = b.z; ov[7] = b.w;
+            } else {
+                const uint4 ow = *reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(o) + base);
+                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ow);
 #pragma unroll
-            for (int e = 0; e < E; ++e) ov[e] = op[e];
-        } else {
-            const __nv_bfloat16* op = static_cast<const __nv_bfloat16*>(o) + base;
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(o2[e]);
+                    ov[2 * e] = f.x;
+                    ov[2 * e + 1] = f.y;
+                }
+            }
 #pragma unroll
-            for (int e = 0; e < E; ++e) ov[e] = __bfloat162float(op[e]);
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(d2[e]);
+                acc = fmaf(ov[2 * e], f.x, acc);
+                acc = fmaf(ov[2 * e + 1], f.y, acc);
+            }
+            float4* z = reinterpret_cast<float4*>(dq_acc + base);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int e = 0; e < E; ++e) dv[e] = __bfloat162float(dout[base + e]);
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc = fmaf(ov[e], dv[e], acc);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) Dout[(size_t)h * T + (size_t)t] = acc;
-#pragma unroll
-        for (int e = 0; e < E; ++e) dq_acc[base + e] = 0.f;
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (valid && l == 0) Dout[(size_t)(r % Hq) * T + (size_t)(r / Hq)] = acc;
     }
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    for (long long s = tid; s < n_sems; s += (long long)gridDim.x * blockDim.x) sems[s] = 0;
+    for (long long si = tid; si < n_sems; si += (long long)gridDim.x * blockDim.x) sems[si] = 0;
 }
 
 // dq = scale * dq_acc; for GQA, dk/dv[t,g] = sum over the group's query heads h
@@ -914,7 +940,8 @@ cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, f
                                   float* dq_acc, int* sems, long long n_sems, int T, int Hq,
                                   int d, int num_sms, cudaStream_t stream) {
     const long long rows = (long long)T * Hq;
-    const int grid = grid_for(rows * 32 > n_sems ? rows * 32 : n_sems, 256, num_sms);
+    const long long threads = rows * (d / 8) > n_sems ? rows * (d / 8) : n_sems;
+    const int grid = grid_for(threads, 256, num_sms);
     const __nv_bfloat16* dob = static_cast<const __nv_bfloat16*>(dout);
 #define FA_PRE(DD, FF) \
     bwd_preprocess_kernel<DD, FF><<<grid, 256, 0, stream>>>(o, dob, D, dq_acc, sems, n_sems, T, Hq)
