@@ -498,6 +498,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                            make_sdesc(dsaddr + kk * 2048, 16384, 1024),
                                            make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ,
                                            kk > 0);
+                                // committed here, not after the loop: a commit tracks every
+                                // MMA issued before it, and the drain must not wait for S(c+1)
+                                mma_commit(smem_u32(&sm.dq_full));
+                                mma_commit(smem_u32(&sm.ds_free));
+                                mma_commit(smem_u32(&sm.q_empty[st]));
                                 k_done = true;
                                 continue;
                             }
@@ -509,9 +514,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                         if (!ok) break;
                     }
-                    mma_commit(smem_u32(&sm.dq_full));
-                    mma_commit(smem_u32(&sm.ds_free));
-                    mma_commit(smem_u32(&sm.q_empty[st]));
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&sm.dkv_full));

@@ -24,7 +24,11 @@
 // [256,256+d), O_1 [384,384+d); P_t is written as bf16 over the first 64
 // columns of S_t.
 //
-// Softmax uses exp2 with the scale folded in (s * scale * log2 e).  The O~
+// Softmax uses exp2 with the scale folded in (s * scale * log2 e), packed
+// fp32-pair arithmetic for the scale and the row sum, and 3-input maxima.  All
+// exponentials go to the SFU (ex2): the FlashAttention-4 page (section "Die
+// Kernidee des kooperativen Designs") moves part of them to a polynomial on the
+// FMA units, but on this part that made the forward slower, not faster.  The O~
 // rescale is conditional: the reference max is only moved when the row max
 // grows by more than 8 (a factor 256 in P), which keeps P in range while
 // skipping most rescales; the result is exact because l and O~ always share
@@ -94,6 +98,25 @@ __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
     }
     x.nkv = max(x.n[0], x.n[1]);
     return x;
+}
+
+// P = 2^(s * c - m) for one 32-column chunk of a row, packed to bf16 pairs, and
+// its fp32 row sum accumulated in two packed accumulators.  Masked columns hold
+// s = -inf, which ex2 takes to exactly 0.
+__device__ __forceinline__ void softmax_chunk(const float* sc, float c, float neg,
+                                              uint64_t (&acc)[2], uint32_t (&pk)[16]) {
+    const uint64_t c2 = f2_pack(c, c), n2 = f2_pack(neg, neg);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint64_t x = f2_fma(f2_pack(sc[2 * i], sc[2 * i + 1]), c2, n2);
+        float x0, x1;
+        f2_unpack(x, x0, x1);
+        const uint64_t e = f2_pack(ex2_approx(x0), ex2_approx(x1));
+        acc[i & 1] = f2_add(acc[i & 1], e);
+        float p0, p1;
+        f2_unpack(e, p0, p1);
+        pk[i] = pack_bf16x2(p0, p1);
+    }
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* flag, WsHeader* hdr, int code) {
@@ -360,14 +383,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int i = 0; i < 128; ++i)
                         if (i >= thr) s[i] = -INFINITY;
                 }
-                // row max as an 8-way tree (short dependency chains)
+                // row max: 8 independent chains of 3-input maxima
                 float m8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) m8[k] = s[k];
+                for (int k = 0; k < 8; ++k) {
+                    float m = fmax3(s[k], s[8 + k], s[16 + k]);
 #pragma unroll
-                for (int i = 8; i < 128; ++i) m8[i & 7] = fmaxf(m8[i & 7], s[i]);
-                float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    for (int i = 24; i < 120; i += 16) m = fmax3(m, s[i + k], s[i + 8 + k]);
+                    m8[k] = fmaxf(m, s[120 + k]);
+                }
+                float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                 fmaxf(m8[6], m8[7]));
                 mx *= p.scale_log2;
                 float alpha = 1.f;
                 bool need = false;
@@ -380,20 +406,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     l *= alpha;
                 }
                 const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-                float l4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in 4 independent chains
+                uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], p.scale_log2, neg));
-                        const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], p.scale_log2, neg));
-                        l4[i & 3] += p0 + p1;
-                        pk[i] = pack_bf16x2(p0, p1);
-                    }
+                    softmax_chunk(s + c * 32, p.scale_log2, neg, acc, pk);
                     tmem_st16(s_addr + c * 16, pk);
                 }
-                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+                {
+                    float a0, a1, b0, b1;
+                    f2_unpack(acc[0], a0, a1);
+                    f2_unpack(acc[1], b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                }
                 if (__any_sync(0xffffffffu, need)) {
                     // O~ is stable here: S_t(j) was committed after O_t += P_t V of j-1.
 #pragma unroll 1
