@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         while (!(dp_done && dv_done)) {
                             if (!dp_done &&
                                 (!Cfg::kDqAliasesDp || cnt == 0 ||
-                                 mbar_try_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
+                                 mbar_test_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
                                 tc_fence_after();
 #pragma unroll
                                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -431,9 +431,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 dp_done = true;
                                 continue;
                             }
-                            if (!dv_done && mbar_try_wait(smem_u32(&sm.p_ready), cnt & 1) &&
+                            if (!dv_done && mbar_test_wait(smem_u32(&sm.p_ready), cnt & 1) &&
                                 (s != 0 || unit_it == 0 ||
-                                 mbar_try_wait(smem_u32(&sm.dkv_free), (unit_it - 1) & 1))) {
+                                 mbar_test_wait(smem_u32(&sm.dkv_free), (unit_it - 1) & 1))) {
                                 tc_fence_after();
                                 // P^T of query columns [64h, 64h+64) sits in TMEM
                                 // columns [64h, 64h+32)
@@ -465,9 +465,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const uint64_t t_start = globaltimer();
                         while (!(s_done && k_done)) {
                             if (!s_done &&
-                                mbar_try_wait(smem_u32(&sm.q_full[(cnt + 1) & 1]),
+                                mbar_test_wait(smem_u32(&sm.q_full[(cnt + 1) & 1]),
                                               ((cnt + 1) >> 1) & 1) &&
-                                mbar_try_wait(smem_u32(&sm.s_free), cnt & 1)) {
+                                mbar_test_wait(smem_u32(&sm.s_free), cnt & 1)) {
                                 tc_fence_after();
                                 const uint32_t qn = smem_u32(sm.q[(cnt + 1) & 1]);
 #pragma unroll
@@ -480,9 +480,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 s_done = true;
                                 continue;
                             }
-                            if (!k_done && mbar_try_wait(smem_u32(&sm.ds_ready), cnt & 1) &&
+                            if (!k_done && mbar_test_wait(smem_u32(&sm.ds_ready), cnt & 1) &&
                                 (Cfg::kDqAliasesDp || cnt == 0 ||
-                                 mbar_try_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
+                                 mbar_test_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
                                 tc_fence_after();
                                 // dK_j += dS^T Q ; dQ = dS K_j  (A = dS^T in shared memory)
 #pragma unroll
