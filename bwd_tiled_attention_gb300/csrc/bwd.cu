@@ -25,10 +25,10 @@
 //   warp 0       producer: K_j, V_j once per unit, then Q_i with LSE_i, D_i
 //                (2-stage ring) and dO_i (1 stage) by TMA / plain loads
 //   warp 1       MMA issuer (tcgen05, one thread).  Per step: dP and dV in the
-//                order their inputs arrive, then S of the NEXT step as soon as
-//                dV has released the S columns, then dK and dQ once dS is in
-//                shared memory -- so the compute warps find S(i+1) ready when
-//                they finish dS(i)
+//                order their inputs arrive, then dQ once dS is in shared memory,
+//                S of the NEXT step as soon as dV has released the S columns, and
+//                dK last (it only accumulates) -- so the dQ drain starts early and
+//                the compute warps find S(i+1) ready when they finish dS(i)
 //   warp 2       TMEM allocation
 //   warps 4..11  compute, two warpgroups splitting the 128 query columns of a
 //                step into halves; one thread per (key row, half): P^T = exp2(S^T*c - LSE2),
@@ -267,9 +267,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int n_qtiles = hdr->n_qtiles;
     // Registers: the launch gives every thread 128 (512 x 128 = 65536).  The
     // producer/MMA warpgroup (warps 0..3) gives back to 80 at the top of each
-    // role, and the three math warpgroups take 144 each:
-    // 128*80 + 384*144 = 65536 exactly.
-    static_assert(128 * 80 + 384 * 144 == kBwdThreads * 128, "register split must match the launch");
+    // role, the two compute warpgroups keep 128 and the dQ drain warpgroup takes
+    // 176 (it holds a whole 128-column dQ row): 128*80 + 256*128 + 128*176 = 65536.
+    static_assert(128 * 80 + 256 * 128 + 128 * 176 == kBwdThreads * 128,
+                  "register split must match the launch");
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -456,17 +457,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (!ok) break;
                     }
                     mma_commit(smem_u32(&sm.do_empty));  // dO read by dP and dV
-                    // Then the next step's S (needs Q(c+1) and dV(c) done with the S
-                    // columns) and this step's dK/dQ (need dS in shared memory), in
-                    // whichever order their inputs arrive; S first when both are, since
-                    // the compute warps start the next step with it.
+                    // Then this step's dQ, the next step's S and this step's dK, in
+                    // that priority as their inputs arrive.  dQ is on the critical
+                    // loop dQ -> drain -> dP(c+1) -> dS(c+1) -> dQ(c+1); S(c+1) needs
+                    // Q(c+1) and dV(c) done with the S columns; dK only accumulates
+                    // until the unit ends, so it goes last.
                     {
-                        bool s_done = s + 1 >= x.ni, k_done = false;
+                        bool s_done = s + 1 >= x.ni, q_done = false, k_done = false;
                         const uint64_t t_start = globaltimer();
-                        while (!(s_done && k_done)) {
+                        while (!(s_done && q_done && k_done)) {
+                            if (!q_done && mbar_test_wait(smem_u32(&sm.ds_ready), cnt & 1) &&
+                                (Cfg::kDqAliasesDp || cnt == 0 ||
+                                 mbar_test_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
+                                tc_fence_after();
+                                // dQ = dS K_j  (A = dS^T in shared memory read as MN-major)
+#pragma unroll
+                                for (int kk = 0; kk < kTile / 16; ++kk)
+                                    mma_ss(tmem + Cfg::kColDQ,
+                                           make_sdesc(dsaddr + kk * 2048, 16384, 1024),
+                                           make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ,
+                                           kk > 0);
+                                // committed at once: a commit tracks every MMA issued before
+                                // it, and the drain must not wait for later ones
+                                mma_commit(smem_u32(&sm.dq_full));
+                                q_done = true;
+                                continue;
+                            }
                             if (!s_done &&
                                 mbar_test_wait(smem_u32(&sm.q_full[(cnt + 1) & 1]),
-                                              ((cnt + 1) >> 1) & 1) &&
+                                               ((cnt + 1) >> 1) & 1) &&
                                 mbar_test_wait(smem_u32(&sm.s_free), cnt & 1)) {
                                 tc_fence_after();
                                 const uint32_t qn = smem_u32(sm.q[(cnt + 1) & 1]);
@@ -480,11 +499,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 s_done = true;
                                 continue;
                             }
-                            if (!k_done && mbar_test_wait(smem_u32(&sm.ds_ready), cnt & 1) &&
-                                (Cfg::kDqAliasesDp || cnt == 0 ||
-                                 mbar_test_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
-                                tc_fence_after();
-                                // dK_j += dS^T Q ; dQ = dS K_j  (A = dS^T in shared memory)
+                            if (!k_done && q_done) {
+                                // dK_j += dS^T Q  (A = dS^T in shared memory, K-major)
 #pragma unroll
                                 for (int kk = 0; kk < kTile / 16; ++kk) {
                                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -492,17 +508,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                            make_sdesc(qaddr + kk * 2048, 16384, 1024), idKV,
                                            (s > 0 || kk > 0) ? 1u : 0u);
                                 }
-#pragma unroll
-                                for (int kk = 0; kk < kTile / 16; ++kk)
-                                    mma_ss(tmem + Cfg::kColDQ,
-                                           make_sdesc(dsaddr + kk * 2048, 16384, 1024),
-                                           make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ,
-                                           kk > 0);
-                                // committed here, not after the loop: a commit tracks every
-                                // MMA issued before it, and the drain must not wait for S(c+1)
-                                mma_commit(smem_u32(&sm.dq_full));
-                                mma_commit(smem_u32(&sm.ds_free));
-                                mma_commit(smem_u32(&sm.q_empty[st]));
+                                mma_commit(smem_u32(&sm.ds_free));       // dS read by dQ and dK
+                                mma_commit(smem_u32(&sm.q_empty[st]));   // Q(c) read by S(c), dK
                                 k_done = true;
                                 continue;
                             }
@@ -525,7 +532,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ compute: P^T and dS^T
-        setmaxnreg_inc<144>();
+        // (keeps the launch's 128 registers)
         const int q4 = warp & 3;
         const int hc = (warp - 4) >> 2;                   // query-column half of this warpgroup
         const int rk = q4 * 32 + lane;                    // key row within the tile (TMEM lane)
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ drain + dK/dV epilogue
-        setmaxnreg_inc<144>();
+        setmaxnreg_inc<176>();
         const int q4 = warp & 3;
         const int rr = q4 * 32 + lane;  // row within the tile (TMEM lane)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -671,56 +678,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     sem_ok = named_bar_and(1, 128, sem_ok);
                 }
                 const int row0 = i * kTile;
-                // dQ row in halves of 64 columns; the TMEM columns go back as soon as
-                // the last half is in registers (the next dP MMA waits for them).
+                // The whole dQ row goes to registers first and its TMEM columns go
+                // back at once: the next step's dP MMA waits for them.
                 const bool whole = row0 + kTile <= x.L;
                 const int qr = row0 + rr;
+                uint32_t v[D / 32][32];
 #pragma unroll
-                for (int hf = 0; hf < D / 64; ++hf) {
-                    uint32_t v[2][32];
-                    tmem_ld32(tmem + lane_off + Cfg::kColDQ + hf * 64, v[0]);
-                    tmem_ld32(tmem + lane_off + Cfg::kColDQ + hf * 64 + 32, v[1]);
-                    tmem_ld_wait();
-                    if (hf == D / 64 - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
+                for (int cc = 0; cc < D / 32; ++cc)
+                    tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v[cc]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
+                if (whole) {
+                    // Whole tile: bulk reduce-add, one 32-column chunk at a time,
+                    // staged 128B-swizzled through two 16 KB slots.
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc, ++chunk) {
+                        const int sl = chunk & 1;
+                        // the reduce that last used this slot has read it
+                        if (leader) bulk_wait_group_read<1>();
+                        named_bar_sync(1, 128);
+                        uint8_t* row = stage_row + sl * (kTile * 128);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) =
+                                make_uint4(v[cc][4 * e], v[cc][4 * e + 1], v[cc][4 * e + 2],
+                                           v[cc][4 * e + 3]);
+                        fence_proxy_async_smem();
+                        named_bar_sync(1, 128);
+                        if (leader && sem_ok)
+                            tma_reduce_add_3d(&p.tm_dq_acc, stage_base + sl * (kTile * 128), cc * 32,
+                                              x.h, x.t0 + row0);
+                        if (leader) bulk_commit_group();
                     }
-                    if (whole) {
-                        // Whole tile: bulk reduce-add, one 32-column chunk at a time,
-                        // staged 128B-swizzled through two 16 KB slots.
+                } else if (qr < x.L && sem_ok) {
+                    // Ragged last tile of a sequence: per-row vector reductions.
+                    float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h, ++chunk) {
-                            const int cc = hf * 2 + h;
-                            const int sl = chunk & 1;
-                            // the reduce that last used this slot has read it
-                            if (leader) bulk_wait_group_read<1>();
-                            named_bar_sync(1, 128);
-                            uint8_t* row = stage_row + sl * (kTile * 128);
+                    for (int cc = 0; cc < D / 32; ++cc)
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) =
-                                    make_uint4(v[h][4 * e], v[h][4 * e + 1], v[h][4 * e + 2],
-                                               v[h][4 * e + 3]);
-                            fence_proxy_async_smem();
-                            named_bar_sync(1, 128);
-                            if (leader && sem_ok)
-                                tma_reduce_add_3d(&p.tm_dq_acc, stage_base + sl * (kTile * 128),
-                                                  cc * 32, x.h, x.t0 + row0);
-                            if (leader) bulk_commit_group();
-                        }
-                    } else if (qr < x.L && sem_ok) {
-                        // Ragged last tile of a sequence: per-row vector reductions.
-                        float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D + hf * 64;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                red_add_v4(dst + h * 32 + 4 * e, __uint_as_float(v[h][4 * e]),
-                                           __uint_as_float(v[h][4 * e + 1]),
-                                           __uint_as_float(v[h][4 * e + 2]),
-                                           __uint_as_float(v[h][4 * e + 3]));
-                    }
+                        for (int e = 0; e < 8; ++e)
+                            red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[cc][4 * e]),
+                                       __uint_as_float(v[cc][4 * e + 1]),
+                                       __uint_as_float(v[cc][4 * e + 2]),
+                                       __uint_as_float(v[cc][4 * e + 3]));
                 }
                 if (p.deterministic) {
                     // this contribution must be complete before the next one may start
