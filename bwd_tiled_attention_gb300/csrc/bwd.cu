@@ -23,7 +23,8 @@
 //
 // Roles (512 threads):
 //   warp 0       producer: K_j, V_j once per unit, then Q_i with LSE_i, D_i
-//                (2-stage ring) and dO_i (1 stage) by TMA / plain loads
+//                (2-stage ring) by TMA / plain loads
+//   warp 3       dO producer: dO_i (1 stage) by TMA, as soon as its slot frees
 //   warp 1       MMA issuer (tcgen05, one thread).  Per step: dP and dV in the
 //                order their inputs arrive, then dQ once dS is in shared memory,
 //                S of the NEXT step as soon as dV has released the S columns, and
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&sm.sched_full[i]), 1);
-            mbar_init(smem_u32(&sm.sched_empty[i]), 1 + 12);
+            mbar_init(smem_u32(&sm.sched_empty[i]), 2 + 12);
             mbar_init(smem_u32(&sm.q_full[i]), 1 + 32);
             mbar_init(smem_u32(&sm.q_empty[i]), 1);
         }
@@ -341,16 +342,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     sm.dd[st][rr] = dv;
                 }
                 mbar_arrive(qbar);
-                // dO_i into its single stage, once dP and dV of the previous step ran
-                if (!(ok = lane0_wait(smem_u32(&sm.do_empty), (c & 1) ^ 1, abort_flag, hdr)))
-                    break;
-                if (lane == 0) {
-                    const uint32_t dbar = smem_u32(&sm.do_full);
-                    mbar_arrive_expect_tx(dbar, Cfg::kTileBytes);
-                    for (int cb = 0; cb < Cfg::kBoxes; ++cb)
-                        tma_load_3d(smem_u32(sm.dout) + cb * 16384, &p.tm_do, dbar, cb * 64, x.h,
-                                    x.t0 + i * kTile);
-                }
             }
         }
         if (lane == 0) {
@@ -360,8 +351,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int it = c - 1 - e;
                 mbar_wait(smem_u32(&sm.q_full[it & 1]), (it >> 1) & 1, z);
             }
-            if (c > 0) mbar_wait(smem_u32(&sm.do_full), (c - 1) & 1, z);
             if (unit_it > 0) mbar_wait(smem_u32(&sm.kv_full), (unit_it - 1) & 1, z);
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ dO producer
+        // dO_i into its single stage as soon as dP and dV of the previous step
+        // have read it, independent of the Q ring's pace
+        setmaxnreg_dec<80>();
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_do);
+            int sched_it = 0, c = 0;
+            bool ok = true;
+            while (ok) {
+                const int slot = sched_it & 1;
+                if (!(ok = wait_or_abort(smem_u32(&sm.sched_full[slot]), (sched_it >> 1) & 1,
+                                         abort_flag, hdr)))
+                    break;
+                const int2 unit = sm.sched[slot];
+                mbar_arrive(smem_u32(&sm.sched_empty[slot]));
+                ++sched_it;
+                if (unit.x < 0) break;
+                const BUnit x = decode_bunit(unit, p);
+                for (int s = 0; s < x.ni; ++s, ++c) {
+                    const int i = walk_tile(x, s, p.deterministic, p.causal);
+                    if (!(ok = wait_or_abort(smem_u32(&sm.do_empty), (c & 1) ^ 1, abort_flag, hdr)))
+                        break;
+                    const uint32_t dbar = smem_u32(&sm.do_full);
+                    mbar_arrive_expect_tx(dbar, Cfg::kTileBytes);
+                    for (int cb = 0; cb < Cfg::kBoxes; ++cb)
+                        tma_load_3d(smem_u32(sm.dout) + cb * 16384, &p.tm_do, dbar, cb * 64, x.h,
+                                    x.t0 + i * kTile);
+                }
+            }
+            // never leave a TMA write in flight
+            if (c > 0) mbar_wait(smem_u32(&sm.do_full), (c - 1) & 1, &sm.zero);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -800,7 +823,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // the staging slots must not be read after the CTA exits
         if (leader) bulk_wait_group<0>();
     } else {
-        setmaxnreg_dec<80>();  // warps 2 and 3: TMEM allocation only
+        setmaxnreg_dec<80>();  // warp 2: TMEM allocation only
     }
 
     tc_fence_before();
