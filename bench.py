@@ -267,19 +267,22 @@ def main():
         if st != fa.FA_OK:
             raise fa.FAError(st, what)
 
-    def step(events=None):
+    def step(events=None, xin=None, grads=None):
+        xi = x if xin is None else xin
+        gq, gk, gv = (dq, dk, dv) if grads is None else grads
         if events:
             events[0].record(stream)
-        check(fa.fa_fwd(x["q"], x["k"], x["v"], o, fa.FA_BF16, lse, B, Hq, Hkv, N, T, d, scale,
+        check(fa.fa_fwd(xi["q"], xi["k"], xi["v"], o, fa.FA_BF16, lse, B, Hq, Hkv, N, T, d, scale,
                         w.causal, cu, fws, fws_b, stream), "fa_fwd")
         if events:
             events[1].record(stream)
-        check(fa.fa_bwd_preprocess(o, fa.FA_BF16, x["dout"], Dv, bws, bws_b, B, Hq, Hkv, N, T, d,
+        check(fa.fa_bwd_preprocess(o, fa.FA_BF16, xi["dout"], Dv, bws, bws_b, B, Hq, Hkv, N, T, d,
                                    w.causal, cu, det, stream), "fa_bwd_preprocess")
         if events:
             events[2].record(stream)
-        check(fa.fa_bwd(x["q"], x["k"], x["v"], x["dout"], lse, Dv, dq, dk, dv, fa.FA_BF16, bws,
-                        bws_b, B, Hq, Hkv, N, T, d, scale, w.causal, cu, det, stream), "fa_bwd")
+        check(fa.fa_bwd(xi["q"], xi["k"], xi["v"], xi["dout"], lse, Dv, gq, gk, gv, fa.FA_BF16,
+                        bws, bws_b, B, Hq, Hkv, N, T, d, scale, w.causal, cu, det, stream),
+              "fa_bwd")
         if events:
             events[3].record(stream)
 
@@ -314,25 +317,51 @@ def main():
     value, total_ms = job_throughput((fl_f + fl_b) * K, sum(t_step), dist, dev)
     ms_per_step = total_ms / K
 
-    # end to end through the public API with host buffers: H2D inputs, fwd+bwd, D2H grads
+    # End to end through the public API with host buffers: every step copies
+    # its inputs host -> device, runs fwd + bwd and copies the gradients back.
+    # The copies run on their own streams with two buffer sets, so step i+1's
+    # upload and step i-1's download overlap step i's compute; events keep
+    # each buffer's writer after its last reader.
     host_in = {k: inp[k].pin_memory() for k in ("q", "k", "v", "dout")}
-    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+                for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    xs = [x, {k: torch.empty_like(x[k]) for k in x}]
+    gs = [(dq, dk, dv), tuple(torch.empty_like(t) for t in (dq, dk, dv))]
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_h2d = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_d2h = [torch.cuda.Event() for _ in range(2)]
     E = args.e2e_steps
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     for i in range(E + 2):
-        if i == 2:
+        sl = i & 1
+        if i == 2:  # the first two steps fill the pipeline, untimed
             torch.cuda.synchronize()
             if dist:
                 dist.barrier()
             e0.record(stream)
-        for k_ in ("q", "k", "v", "dout"):
-            x[k_].copy_(host_in[k_], non_blocking=True)
-        step()
-        for src, dst in zip((dq, dk, dv), host_out):
-            dst.copy_(src, non_blocking=True)
+            s_h2d.wait_event(e0)
+        with torch.cuda.stream(s_h2d):
+            if i >= 2:
+                s_h2d.wait_event(ev_comp[sl])  # step i-2 has read this input set
+            for k_ in ("q", "k", "v", "dout"):
+                xs[sl][k_].copy_(host_in[k_], non_blocking=True)
+            ev_h2d[sl].record(s_h2d)
+        stream.wait_event(ev_h2d[sl])
+        if i >= 2:
+            stream.wait_event(ev_d2h[sl])  # step i-2's gradients have been copied out
+        step(xin=xs[sl], grads=gs[sl])
+        ev_comp[sl].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev_comp[sl])
+            for src, dst in zip(gs[sl], host_out[sl]):
+                dst.copy_(src, non_blocking=True)
+            ev_d2h[sl].record(s_d2h)
+    for sl in range(2):
+        stream.wait_event(ev_d2h[sl])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_value, _ = job_throughput((fl_f + fl_b) * E, e0.elapsed_time(e1), dist, dev)
