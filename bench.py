@@ -33,6 +33,12 @@ if ROOT not in sys.path:
 import synth  # noqa: E402  (input generator: no attention arithmetic)
 
 METRIC = "attention fwd+bwd BF16 TFLOPs/s (hd128, causal) and % of GB300 dense BF16 peak"
+
+# DRAM bytes (read + write) of one fa_bwd call -- the backward kernel and its
+# dQ conversion -- from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum) of this bench's own command on the same workload,
+# for the kernels as they are; a workload without a capture reports null.
+FA_BWD_DRAM_BYTES = {"mid_causal": 773.8e6}
 NOMINAL_PEAK_TFLOPS = 2250.0
 
 
@@ -388,7 +394,7 @@ def main():
         "roofline": {"bound": "tensor", "kernel": "fa_bwd (backward kernel + dQ conversion)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} bf16 burst",
-                     "traffic": None},
+                     "traffic": FA_BWD_DRAM_BYTES.get(w.name)},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * K,
