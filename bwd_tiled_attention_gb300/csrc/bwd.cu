@@ -212,6 +212,7 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* l
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+    pdl_begin();
     using Cfg = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.workspace);
@@ -842,6 +843,7 @@ __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const void* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                           float* __restrict__ Dout, float* __restrict__ dq_acc,
                           int* __restrict__ sems, long long n_sems, int T, int Hq) {
+    pdl_begin();
     constexpr int LPR = D / 8;     // lanes per row
     constexpr int RPW = 32 / LPR;  // rows per warp pass
     const long long rows = (long long)T * Hq;
@@ -902,6 +904,7 @@ __global__ void __launch_bounds__(256)
                            const float* __restrict__ dk_acc, const float* __restrict__ dv_acc,
                            void* __restrict__ dk, void* __restrict__ dv, int T, int Hq, int Hkv,
                            float scale) {
+    pdl_begin();
     constexpr int V = D / 4;  // float4 groups per row
     const long long nq = (long long)T * Hq * V;
     const long long nkv = dk_acc ? (long long)T * Hkv * V : 0;
@@ -957,8 +960,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, int num_sms, cudaStream_t stream) {
     const long long bound = max_tiles(p.B, p.T, kTile) * p.Hq;
     const int grid = (int)(bound < num_sms ? bound : num_sms);
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, kBwdThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kBwdThreads), smem, stream, p);
 }
 
 }  // namespace
@@ -970,15 +972,17 @@ cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, f
     const long long threads = rows * (d / 8) > n_sems ? rows * (d / 8) : n_sems;
     const int grid = grid_for(threads, 256, num_sms);
     const __nv_bfloat16* dob = static_cast<const __nv_bfloat16*>(dout);
-#define FA_PRE(DD, FF) \
-    bwd_preprocess_kernel<DD, FF><<<grid, 256, 0, stream>>>(o, dob, D, dq_acc, sems, n_sems, T, Hq)
+    cudaError_t e;
+#define FA_PRE(DD, FF)                                                                  \
+    e = launch_pdl(bwd_preprocess_kernel<DD, FF>, dim3(grid), dim3(256), 0, stream, o, dob, D, \
+                   dq_acc, sems, n_sems, T, Hq)
     if (d == 128) {
         if (o_fp32) FA_PRE(128, true); else FA_PRE(128, false);
     } else {
         if (o_fp32) FA_PRE(64, true); else FA_PRE(64, false);
     }
 #undef FA_PRE
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream) {
@@ -991,16 +995,17 @@ cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const float* d
                                    cudaStream_t stream) {
     const long long work = (long long)T * (Hq + (dk_acc ? 2 * Hkv : 0)) * d / 4;
     const int grid = grid_for(work, 256, num_sms);
-#define FA_POST(DD, FF)                                                                         \
-    bwd_postprocess_kernel<DD, FF><<<grid, 256, 0, stream>>>(dq_acc, dq, dk_acc, dv_acc, dk, dv, \
-                                                             T, Hq, Hkv, scale)
+    cudaError_t e;
+#define FA_POST(DD, FF)                                                                   \
+    e = launch_pdl(bwd_postprocess_kernel<DD, FF>, dim3(grid), dim3(256), 0, stream, dq_acc, dq, \
+                   dk_acc, dv_acc, dk, dv, T, Hq, Hkv, scale)
     if (d == 128) {
         if (grad_fp32) FA_POST(128, true); else FA_POST(128, false);
     } else {
         if (grad_fp32) FA_POST(64, true); else FA_POST(64, false);
     }
 #undef FA_POST
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace fa

@@ -2,8 +2,11 @@
 // tile sizes, workspace layouts, the work-unit encoding written by the tile
 // scheduler, and per-sequence geometry.
 #pragma once
+#include <cuda_runtime.h>
+
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 namespace fa {
 
@@ -31,6 +34,33 @@ __host__ __device__ inline int make_unit_y(int tile, int head) { return (tile <<
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation allowed, and its first two instructions
+// let the next kernel in the stream be scheduled at once and then wait until
+// the previous kernel has completed and its memory is visible.  So a kernel
+// never reads its predecessor's output early; what overlaps is the launch
+// latency of the next grid.  Outside such a launch both are no-ops.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Upper bound on tiles of `rows` rows over all sequences of a batch:
 // sum_b ceil(L_b / rows) <= ceil(T / rows) + B.

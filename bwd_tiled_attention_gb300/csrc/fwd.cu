@@ -140,6 +140,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <int D, bool OUT_FP32>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+    pdl_begin();
     using Cfg = FwdCfg<D>;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -506,8 +507,7 @@ cudaError_t launch_fwd_t(const FwdParams& p, int num_sms, cudaStream_t stream) {
     const long long bound = max_tiles(p.B, p.T, kFwdBlockRows) * p.Hq;
     const int grid = (int)(bound < num_sms ? bound : num_sms);
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, kFwdThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kFwdThreads), smem, stream, p);
 }
 
 }  // namespace

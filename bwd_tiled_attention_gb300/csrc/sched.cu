@@ -53,6 +53,7 @@ __device__ __forceinline__ int find_slot(const long long* prefix, int n, long lo
 }
 
 __global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedArgs a) {
+    pdl_begin();
     extern __shared__ __align__(16) unsigned char sm[];
     const int tid = threadIdx.x;
     const int B = a.B, H = a.H;
@@ -213,8 +214,7 @@ cudaError_t launch_sched(const int* cu_seqlens, int B, int N, int H, int rows, i
                                              (int)smem);
         if (e != cudaSuccess) return e;
     }
-    sched_kernel<<<1, kSchedThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(sched_kernel, dim3(1), dim3(kSchedThreads), smem, stream, a);
 }
 
 }  // namespace fa
