@@ -212,11 +212,12 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* l
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
-    pdl_begin();
+    pdl_trigger();
     using Cfg = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.workspace);
     if (smem_u32(smem_raw) & 1023u) {  // layout relies on a 1024-byte aligned base
+        pdl_wait();
         if (threadIdx.x == 0) atomicOr(&hdr->error, kErrSmemAlign);
         return;
     }
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    pdl_wait();  // the unit list, LSE, D and the reset workspace are the previous kernels' output
     const int n_units = hdr->n_units;
     const int n_qtiles = hdr->n_qtiles;
     // Registers: the launch gives every thread 128 (512 x 128 = 65536).  The

@@ -36,14 +36,19 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 // Programmatic dependent launch.  Every kernel of the library is launched with
-// programmatic stream serialisation allowed, and its first two instructions
-// let the next kernel in the stream be scheduled at once and then wait until
-// the previous kernel has completed and its memory is visible.  So a kernel
-// never reads its predecessor's output early; what overlaps is the launch
-// latency of the next grid.  Outside such a launch both are no-ops.
-__device__ __forceinline__ void pdl_begin() {
+// programmatic stream serialisation allowed.  It first lets the next kernel in
+// the stream be scheduled (pdl_trigger), and waits until the previous kernel
+// has completed and its memory is visible (pdl_wait) before it touches any
+// global memory; the persistent kernels set up barriers and TMEM in between.
+// So no kernel reads its predecessor's output early; what overlaps is the
+// next grid's launch and set-up.  Outside such a launch both are no-ops.
+__device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+    pdl_trigger();
+    pdl_wait();
 }
 
 template <typename... KArgs, typename... Args>

@@ -140,7 +140,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <int D, bool OUT_FP32>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-    pdl_begin();
+    pdl_trigger();
     using Cfg = FwdCfg<D>;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    pdl_wait();  // the unit list and inputs are the previous kernels' output
     const int n_units = hdr->n_units;
     // Registers: the launch gives every thread 168 (384 x 168 = 64512).  The
     // producer/MMA warpgroup (warps 0..3) needs few, so each of its warps gives
