@@ -209,7 +209,9 @@ fa_status fa_bwd_preprocess(const void* o, fa_dtype o_dtype, const void* dout, f
     const int nsm = sm_count();
     if (nsm <= 0) return FA_ERR_CUDA;
     cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
-    const int order = !causal ? kOrderSeqDesc : (deterministic ? kOrderLevelDesc : kOrderWorkDesc);
+    // deterministic: descending key/value tile, the order of every dQ tile's
+    // contributions; atomic: heaviest first
+    const int order = deterministic ? kOrderLevelDesc : (causal ? kOrderWorkDesc : kOrderSeqDesc);
     char* ws = static_cast<char*>(workspace);
     cudaError_t e = launch_sched(cu_seqlens, B, N, Hq, kTile, order, lay.max_units, workspace,
                                  lay.units, lay.tile_off, true, strm);

@@ -12,14 +12,17 @@
 // memory, either with fp32 atomics or -- deterministic mode, section 3.2 of
 // the same page -- in a fixed order enforced by one semaphore per dQ tile.
 //
-// Walk order (section 3.3.1): in deterministic mode unit j visits query tiles
-// i = j, j+1, ... (wrapping around for non-causal attention), so the
-// contribution of unit j to dQ tile i is the ((i - j) mod n)-th one,
-// contributions to a tile arrive in descending j, and under the causal mask no
-// unit waits on its first dQ write; the scheduler launches units with
-// descending j.  In atomic mode all units of a (sequence, head) walk the query
-// tiles in one common order (for L2 reuse of Q, dO and the dQ accumulator) and
-// are launched heaviest-first.
+// Walk order (section 3.3.1): in deterministic mode the scheduler launches
+// units with descending j and every dQ tile takes its contributions in
+// descending j, so a unit only ever waits on units taken from the work counter
+// before it (no deadlock at any size, whatever CTA holds which unit).  Under
+// the causal mask unit j visits query tiles i = j, j+1, ..., so its
+// contribution to tile i is the (i - j)-th, unit j+1 wrote the same tile one
+// step earlier and no unit waits on its first dQ write.  Without the mask all
+// units walk i = 0, 1, ... and unit j's contribution is the (n - 1 - j)-th.
+// In atomic mode all units of a (sequence, head) walk the query tiles in one
+// common order (for L2 reuse of Q, dO and the dQ accumulator) and are
+// launched heaviest-first.
 //
 // Roles (512 threads):
 //   warp 0       producer: K_j, V_j once per unit, then Q_i with LSE_i, D_i
@@ -110,19 +113,23 @@ __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
 }
 
 // Query tile visited at step s of unit x.
-//  - deterministic mode: i = j, j+1, ... (wrapping for non-causal), so unit j's
-//    contribution to tile i is the ((i - j) mod n)-th and no unit waits on its
-//    first dQ write;
-//  - atomic mode: every unit of a (sequence, head) walks the tiles in the same
-//    order -- descending from the last tile under the causal mask, ascending
-//    otherwise -- so units running side by side load the same Q/dO tile and
-//    reduce into the same dQ tile while it is resident in L2.
+//  - deterministic causal: i = j, j+1, ..., so unit j's contribution to tile i
+//    is the (i - j)-th and no unit waits on its first dQ write;
+//  - deterministic non-causal and atomic non-causal: i = 0, 1, ...;
+//  - atomic causal: descending from the last tile.
+// In atomic mode every unit of a (sequence, head) walks the tiles in the same
+// order, so units running side by side load the same Q/dO tile and reduce into
+// the same dQ tile while it is resident in L2.
 __device__ __forceinline__ int walk_tile(const BUnit& x, int s, int deterministic, int causal) {
-    if (deterministic) {
-        const int i = x.j + s;
-        return i >= x.nt ? i - x.nt : i;
-    }
-    return causal ? x.nt - 1 - s : s;
+    if (!causal) return s;
+    return deterministic ? x.j + s : x.nt - 1 - s;
+}
+
+// Deterministic mode: how many contributions to dQ tile i precede unit x's.
+// Contributions arrive in descending key/value tile: under the causal mask
+// tile i receives them from units i, i-1, ..., 0; without it from n-1, ..., 0.
+__device__ __forceinline__ int dq_rank(const BUnit& x, int i, int causal) {
+    return causal ? i - x.j : x.nt - 1 - x.j;
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* flag, WsHeader* hdr, int code) {
@@ -696,9 +703,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (p.deterministic) {
                     sem = sems + (size_t)x.h * n_qtiles + tile_off[x.b] + i;
                     if (leader) {
-                        int target = i - x.j;
-                        if (target < 0) target += x.nt;
-                        sem_ok = sem_wait(sem, target, hdr);
+                        sem_ok = sem_wait(sem, dq_rank(x, i, p.causal), hdr);
                         if (!sem_ok) raise_abort(abort_flag, hdr, kErrTimeout);
                     }
                     sem_ok = named_bar_and(1, 128, sem_ok);

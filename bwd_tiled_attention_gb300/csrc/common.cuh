@@ -129,8 +129,9 @@ __device__ __forceinline__ void seq_bounds(const int* cu_seqlens, int N, int b, 
 
 // Orders the scheduler can write.
 enum SchedOrder : int {
-    kOrderLevelDesc = 0,   // causal: tile index descending across sequences (heaviest
-                           // forward query blocks first; lightest backward KV tiles first)
+    kOrderLevelDesc = 0,   // tile index descending across sequences: causal forward
+                           // (heaviest query blocks first) and deterministic backward
+                           // (the order of every dQ tile's contributions)
     kOrderWorkDesc = 1,    // causal backward, atomic mode: KV tiles by remaining work,
                            // heaviest first (tile index ascending within a sequence)
     kOrderSeqDesc = 2,     // non-causal: sequences longest first, tiles in order
