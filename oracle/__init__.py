@@ -54,18 +54,28 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             lib.oracle_num_threads.restype = ctypes.c_int
-            lib.oracle_attention.restype = ctypes.c_int
-            lib.oracle_attention.argtypes = [_dp] * 10 + [
-                ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int]
-            lib.oracle_rows.restype = ctypes.c_int
-            lib.oracle_rows.argtypes = [_dp] * 4 + [
-                ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip, ctypes.c_int, _dp, _dp, _dp, _dp]
-            lib.oracle_key_grads.restype = ctypes.c_int
-            lib.oracle_key_grads.argtypes = [_dp] * 4 + [
-                ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip, ctypes.c_int, _dp, _dp]
+            for name in ("oracle_attention", "oracle_attention_kv"):
+                f = getattr(lib, name)
+                f.restype = ctypes.c_int
+                f.argtypes = [_dp] * 10 + [ctypes.c_int, _ip] + (
+                    [_ip] if name.endswith("_kv") else []) + [
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int]
+            for name in ("oracle_rows", "oracle_rows_kv"):
+                f = getattr(lib, name)
+                f.restype = ctypes.c_int
+                f.argtypes = [_dp] * 4 + [ctypes.c_int, _ip] + (
+                    [_ip] if name.endswith("_kv") else []) + [
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip, ctypes.c_int, _dp, _dp, _dp,
+                    _dp]
+            for name in ("oracle_key_grads", "oracle_key_grads_kv"):
+                f = getattr(lib, name)
+                f.restype = ctypes.c_int
+                f.argtypes = [_dp] * 4 + [ctypes.c_int, _ip] + (
+                    [_ip] if name.endswith("_kv") else []) + [
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip, ctypes.c_int, _dp, _dp]
             _lib = lib
     return _lib
 
@@ -96,52 +106,66 @@ def _cu(cu_seqlens, T):
     return cu
 
 
-def attention(q, k, v, cu_seqlens, scale, causal, dout=None, heads=None):
+def _cu_pair(cu_seqlens, cu_seqlens_k, Tq, Tk):
+    cu_q = _cu(cu_seqlens, Tq)
+    cu_k = cu_q if cu_seqlens_k is None else _cu(cu_seqlens_k, Tk)
+    if len(cu_k) != len(cu_q):
+        raise ValueError("cu_seqlens and cu_seqlens_k name different batch sizes")
+    return cu_q, cu_k
+
+
+def attention(q, k, v, cu_seqlens, scale, causal, dout=None, heads=None, cu_seqlens_k=None):
     """Forward (and backward when ``dout`` is given) over query heads ``heads``.
 
-    q: [T, Hq, d]; k, v: [T, Hkv, d]; dout: [T, Hq, d] or None.
+    q: [Tq, Hq, d]; k, v: [Tk, Hkv, d]; dout: [Tq, Hq, d] or None.
+    cu_seqlens bounds the query sequences; cu_seqlens_k the key/value
+    sequences (default: the same as cu_seqlens).  With different lengths the
+    causal mask is aligned at the end: query i of Lq sees key j iff
+    j <= i + Lk - Lq.
     heads: (h_lo, h_hi) half-open range of query heads, default all.
-    Returns a dict with o [T,Hq,d], lse [Hq,T] and, for the backward,
-    D [Hq,T], dq [T,Hq,d], dk, dv [T,Hkv,d].  Entries for heads outside the
-    range (and kv heads they do not reach) are left at zero.
+    Returns a dict with o [Tq,Hq,d], lse [Hq,Tq] and, for the backward,
+    D [Hq,Tq], dq [Tq,Hq,d], dk, dv [Tk,Hkv,d].  Entries for heads outside the
+    range (and kv heads they do not reach) are left at zero.  A row that sees
+    no key has O = 0 and LSE = -inf.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
-    T, Hq, d = q.shape
-    Hkv = k.shape[1]
-    assert k.shape == (T, Hkv, d) and v.shape == (T, Hkv, d)
-    cu = _cu(cu_seqlens, T)
+    Tq, Hq, d = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    assert k.shape == (Tk, Hkv, d) and v.shape == (Tk, Hkv, d)
+    cu_q, cu_k = _cu_pair(cu_seqlens, cu_seqlens_k, Tq, Tk)
     h_lo, h_hi = heads if heads is not None else (0, Hq)
-    o = np.zeros((T, Hq, d))
-    lse = np.zeros((Hq, T))
+    o = np.zeros((Tq, Hq, d))
+    lse = np.zeros((Hq, Tq))
     out = {"o": o, "lse": lse}
     D = dq = dk = dv = None
     if dout is not None:
         dout = _f64(dout)
         assert dout.shape == q.shape
-        D = np.zeros((Hq, T))
-        dq = np.zeros((T, Hq, d))
-        dk = np.zeros((T, Hkv, d))
-        dv = np.zeros((T, Hkv, d))
+        D = np.zeros((Hq, Tq))
+        dq = np.zeros((Tq, Hq, d))
+        dk = np.zeros((Tk, Hkv, d))
+        dv = np.zeros((Tk, Hkv, d))
         out.update(D=D, dq=dq, dk=dk, dv=dv)
-    rc = _load().oracle_attention(
+    rc = _load().oracle_attention_kv(
         _p(q), _p(k), _p(v), _p(dout), _p(o), _p(lse), _p(D), _p(dq), _p(dk), _p(dv),
-        len(cu) - 1, cu.ctypes.data_as(_ip), Hq, Hkv, d, float(scale), int(bool(causal)),
-        int(h_lo), int(h_hi))
+        len(cu_q) - 1, cu_q.ctypes.data_as(_ip), cu_k.ctypes.data_as(_ip), Hq, Hkv, d,
+        float(scale), int(bool(causal)), int(h_lo), int(h_hi))
     if rc != 0:
         raise ValueError(f"oracle_attention rejected its arguments (rc={rc})")
     return out
 
 
-def rows(q, k, v, cu_seqlens, scale, causal, b, h, row_idx, dout=None):
+def rows(q, k, v, cu_seqlens, scale, causal, b, h, row_idx, dout=None, cu_seqlens_k=None):
     """O, LSE (and D, dQ when ``dout`` is given) for selected rows of (sequence b, head h).
 
-    row_idx are positions within the sequence.  Returns compact arrays
-    o [n,d], lse [n] and, for the backward, D [n], dq [n,d].
+    row_idx are positions within the query sequence; cu_seqlens_k as in
+    ``attention``.  Returns compact arrays o [n,d], lse [n] and, for the
+    backward, D [n], dq [n,d].
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
-    T, Hq, d = q.shape
+    Tq, Hq, d = q.shape
     Hkv = k.shape[1]
-    cu = _cu(cu_seqlens, T)
+    cu_q, cu_k = _cu_pair(cu_seqlens, cu_seqlens_k, Tq, k.shape[0])
     r = _i32(row_idx)
     n = len(r)
     o = np.zeros((n, d))
@@ -151,10 +175,10 @@ def rows(q, k, v, cu_seqlens, scale, causal, b, h, row_idx, dout=None):
         dout = _f64(dout)
         D = np.zeros(n)
         dq = np.zeros((n, d))
-    rc = _load().oracle_rows(
-        _p(q), _p(k), _p(v), _p(dout), len(cu) - 1, cu.ctypes.data_as(_ip), Hq, Hkv, d,
-        float(scale), int(bool(causal)), int(b), int(h), r.ctypes.data_as(_ip), n,
-        _p(o), _p(lse), _p(D), _p(dq))
+    rc = _load().oracle_rows_kv(
+        _p(q), _p(k), _p(v), _p(dout), len(cu_q) - 1, cu_q.ctypes.data_as(_ip),
+        cu_k.ctypes.data_as(_ip), Hq, Hkv, d, float(scale), int(bool(causal)), int(b), int(h),
+        r.ctypes.data_as(_ip), n, _p(o), _p(lse), _p(D), _p(dq))
     if rc != 0:
         raise ValueError(f"oracle_rows rejected its arguments (rc={rc})")
     res = {"o": o, "lse": lse}
@@ -163,21 +187,22 @@ def rows(q, k, v, cu_seqlens, scale, causal, b, h, row_idx, dout=None):
     return res
 
 
-def key_grads(q, k, v, dout, cu_seqlens, scale, causal, b, g, key_idx):
-    """dK, dV for selected keys (positions within sequence b) of kv head g,
-    summed over all query heads of the group.  Returns dk [n,d], dv [n,d]."""
+def key_grads(q, k, v, dout, cu_seqlens, scale, causal, b, g, key_idx, cu_seqlens_k=None):
+    """dK, dV for selected keys (positions within key sequence b) of kv head g,
+    summed over all query heads of the group; cu_seqlens_k as in
+    ``attention``.  Returns dk [n,d], dv [n,d]."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
-    T, Hq, d = q.shape
+    Tq, Hq, d = q.shape
     Hkv = k.shape[1]
-    cu = _cu(cu_seqlens, T)
+    cu_q, cu_k = _cu_pair(cu_seqlens, cu_seqlens_k, Tq, k.shape[0])
     kk = _i32(key_idx)
     n = len(kk)
     dk = np.zeros((n, d))
     dv = np.zeros((n, d))
-    rc = _load().oracle_key_grads(
-        _p(q), _p(k), _p(v), _p(dout), len(cu) - 1, cu.ctypes.data_as(_ip), Hq, Hkv, d,
-        float(scale), int(bool(causal)), int(b), int(g), kk.ctypes.data_as(_ip), n,
-        _p(dk), _p(dv))
+    rc = _load().oracle_key_grads_kv(
+        _p(q), _p(k), _p(v), _p(dout), len(cu_q) - 1, cu_q.ctypes.data_as(_ip),
+        cu_k.ctypes.data_as(_ip), Hq, Hkv, d, float(scale), int(bool(causal)), int(b), int(g),
+        kk.ctypes.data_as(_ip), n, _p(dk), _p(dv))
     if rc != 0:
         raise ValueError(f"oracle_key_grads failed (rc={rc})")
     return {"dk": dk, "dv": dv}

@@ -350,8 +350,12 @@ MUTATIONS = {
     # (pattern in the C source, replacement): each is a plausible slip
     "dropped_scale_dq": ("dqi[c] += scale * dS * kj[c];", "dqi[c] += dS * kj[c];"),
     "wrong_sign_dS": ("const double dS = P * (dP - D[", "const double dS = P * (D["),
-    "causal_off_by_one": ("const int nv = causal ? (i + 1 < L ? i + 1 : L) : L;",
-                          "const int nv = causal ? (i < L ? i : L) : L;"),
+    "causal_off_by_one": ("nv = i + off + 1;", "nv = i + off;"),
+    # the end-aligned causal offset for different query and key lengths
+    "kv_offset_sign_rows": ("Lk, Lk - Lq, i, g,", "Lk, Lq - Lk, i, g,"),
+    "kv_offset_sign_cols": ("int i0 = causal ? j - off : 0;", "int i0 = causal ? j + off : 0;"),
+    "kv_keys_from_query_base": ("row_s[j] = scale * dot(qi, k + IDX(tk0 + j,",
+                                "row_s[j] = scale * dot(qi, k + IDX(j,"),
     "kv_head_map": ("return (int)(((long long)h * Hkv) / Hq);", "return h % Hkv;"),
     "transposed_dv": ("dvj[c] += P * doi[c];", "dvj[c] += P * qi[c];"),
 }
@@ -378,6 +382,10 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
     lib.oracle_attention.argtypes = [dp] * 10 + [ctypes.c_int, ip, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                                  ctypes.c_int, ctypes.c_int]
+    lib.oracle_attention_kv.restype = ctypes.c_int
+    lib.oracle_attention_kv.argtypes = [dp] * 10 + [ctypes.c_int, ip, ip, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int]
     rng = np.random.default_rng(13)
     lengths = [9, 4]
     Hq, Hkv, d = 4, 2, 5
@@ -391,6 +399,22 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
         lib.oracle_attention(P(q), P(k), P(v), P(do), P(o), P(lse), P(D), P(dq), P(dk), P(dv),
                              2, cu.ctypes.data_as(ip), Hq, Hkv, d, 0.5, int(causal), 0, Hq)
         ref = _torch_reference(q, k, v, do, lengths, Hq, Hkv, 0.5, causal)
+        for got, want in zip((o, lse, dq, dk, dv), ref):
+            if not np.allclose(got, want, atol=1e-9):
+                caught = True
+    # different query and key lengths (queries at the end of the key sequence)
+    from test_oracle_kv_pins import kv_case, torch_reference_kv
+    lq, lk = [3, 6], [8, 6]
+    q, k, v, do, cu_q, cu_k = kv_case(rng, lq, lk, Hq, Hkv, d)
+    Tq, Tk = q.shape[0], k.shape[0]
+    for causal in (False, True):
+        o = np.zeros((Tq, Hq, d)); lse = np.zeros((Hq, Tq)); D = np.zeros((Hq, Tq))
+        dq = np.zeros((Tq, Hq, d)); dk = np.zeros((Tk, Hkv, d)); dv = np.zeros((Tk, Hkv, d))
+        P = lambda a: a.ctypes.data_as(dp)
+        lib.oracle_attention_kv(P(q), P(k), P(v), P(do), P(o), P(lse), P(D), P(dq), P(dk),
+                                P(dv), 2, cu_q.ctypes.data_as(ip), cu_k.ctypes.data_as(ip), Hq,
+                                Hkv, d, 0.5, int(causal), 0, Hq)
+        ref = torch_reference_kv(q, k, v, do, lq, lk, Hq, Hkv, 0.5, causal)
         for got, want in zip((o, lse, dq, dk, dv), ref):
             if not np.allclose(got, want, atol=1e-9):
                 caught = True
