@@ -11,7 +11,10 @@ Layouts (see ``include/fa.h``): q, o, dout, dq ``[T, Hq, d]``; k, v, dk, dv
 ``[T, Hkv, d]``; lse, D ``[Hq, T]`` fp32.  A dense batch of B sequences of
 length N is ``T = B*N`` (pass ``cu_seqlens=None``); a packed variable-length
 batch passes ``cu_seqlens`` (int32 ``[B+1]`` on the device) and the maximum
-length N.
+length N.  Queries and keys may differ in length (``k.shape[0] != q.shape[0]``
+for a dense batch, or ``cu_seqlens_k`` / ``max_seqlen_k`` for a packed one):
+the calls then go to the ``*_kv`` entry points, whose causal mask takes the
+queries to be the last positions of the key sequence.
 """
 from __future__ import annotations
 
@@ -27,7 +30,7 @@ from . import build as _build
 __all__ = [
     "FAError", "lib", "fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_fwd_workspace_size",
     "fa_bwd_workspace_size", "fa_bwd_workspace_semaphore_offset", "fa_check_device_status",
-    "fa_bwd_noalloc",
+    "fa_bwd_noalloc", "fa_fwd_kv", "fa_bwd_kv_workspace_size", "fa_bwd_kv_preprocess", "fa_bwd_kv",
     "fa_status_string", "forward", "backward", "attention", "FA_OK", "FA_ERR_INVALID_ARG",
     "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_BF16", "FA_FP32",
 ]
@@ -58,6 +61,13 @@ _SIGS = {
     "fa_check_device_status": (_i, [_vp, _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                             _i, _i, _f, _i, _vp, _i, _vp]),
+    "fa_fwd_kv": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp,
+                       _vp, _vp, _sz, _vp]),
+    "fa_bwd_kv_workspace_size": (_sz, [_i] * 8),
+    "fa_bwd_kv_preprocess": (_i, [_vp, _i, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _i, _i,
+                                  _i, _vp, _vp, _i, _vp]),
+    "fa_bwd_kv": (_i, [_vp] * 9 + [_i, _vp, _sz, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp,
+                                   _vp, _i, _vp]),
 }
 
 EXPORTED = tuple(_SIGS)
@@ -171,6 +181,38 @@ def fa_bwd_noalloc(q, k, v, o, o_dtype, dout, lse, dq, dk, dv, grad_dtype, B, Hq
                                     _ptr(cu_seqlens), int(bool(deterministic)), _stream(stream)))
 
 
+def fa_fwd_kv(q, k, v, o, o_dtype, lse, B, Hq, Hkv, Nq, total_q, Nk, total_k, d, scale, causal,
+              cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes, stream=None) -> int:
+    return int(lib().fa_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o_dtype), _ptr(lse), B,
+                               Hq, Hkv, Nq, total_q, Nk, total_k, d, float(scale),
+                               int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                               _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def fa_bwd_kv_workspace_size(B, Hq, Hkv, Nq, total_q, Nk, total_k, d) -> int:
+    return int(lib().fa_bwd_kv_workspace_size(B, Hq, Hkv, Nq, total_q, Nk, total_k, d))
+
+
+def fa_bwd_kv_preprocess(o, o_dtype, dout, D, workspace, workspace_bytes, B, Hq, Hkv, Nq,
+                         total_q, Nk, total_k, d, causal, cu_seqlens_q, cu_seqlens_k,
+                         deterministic, stream=None) -> int:
+    return int(lib().fa_bwd_kv_preprocess(_ptr(o), _dt(o_dtype), _ptr(dout), _ptr(D),
+                                          _ptr(workspace), int(workspace_bytes), B, Hq, Hkv, Nq,
+                                          total_q, Nk, total_k, d, int(bool(causal)),
+                                          _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                          int(bool(deterministic)), _stream(stream)))
+
+
+def fa_bwd_kv(q, k, v, dout, lse, D, dq, dk, dv, grad_dtype, workspace, workspace_bytes, B, Hq,
+              Hkv, Nq, total_q, Nk, total_k, d, scale, causal, cu_seqlens_q, cu_seqlens_k,
+              deterministic, stream=None) -> int:
+    return int(lib().fa_bwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(D),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _dt(grad_dtype), _ptr(workspace),
+                               int(workspace_bytes), B, Hq, Hkv, Nq, total_q, Nk, total_k, d,
+                               float(scale), int(bool(causal)), _ptr(cu_seqlens_q),
+                               _ptr(cu_seqlens_k), int(bool(deterministic)), _stream(stream)))
+
+
 def fa_check_device_status(workspace, stream=None) -> int:
     return int(lib().fa_check_device_status(_ptr(workspace), _stream(stream)))
 
@@ -201,61 +243,106 @@ def _geometry(q, k, cu_seqlens, max_seqlen, batch):
     return B, Hq, Hkv, N, T, d
 
 
+def _geometry_kv(q, k, cu_seqlens, max_seqlen, cu_seqlens_k, max_seqlen_k, batch):
+    """(B, Hq, Hkv, Nq, Tq, Nk, Tk, d, kv): kv is True when queries and keys
+    have separate lengths (the *_kv entry points)."""
+    B, Hq, Hkv, Nq, Tq, d = _geometry(q, k, cu_seqlens, max_seqlen, batch)
+    Tk = k.shape[0]
+    if cu_seqlens is None:
+        if cu_seqlens_k is not None:
+            raise ValueError("cu_seqlens_k needs cu_seqlens")
+        Nk = Tk // B if B > 0 else 0
+        if B * Nk != Tk:
+            raise ValueError("Tk must equal B * Nk for a dense batch")
+        return B, Hq, Hkv, Nq, Tq, Nk, Tk, d, Tk != Tq
+    if cu_seqlens_k is None:
+        if Tk != Tq:
+            raise ValueError("keys of another length need cu_seqlens_k")
+        return B, Hq, Hkv, Nq, Tq, Nq, Tk, d, False
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens and cu_seqlens_k name different batch sizes")
+    if max_seqlen_k is None:
+        raise ValueError("cu_seqlens_k needs max_seqlen_k")
+    return B, Hq, Hkv, Nq, Tq, int(max_seqlen_k), Tk, d, True
+
+
 def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, max_seqlen=None, batch=None,
-            out_dtype=torch.bfloat16, stream=None, workspace=None):
+            out_dtype=torch.bfloat16, stream=None, workspace=None, cu_seqlens_k=None,
+            max_seqlen_k=None):
     """Attention forward through the C ABI; returns (o, lse)."""
-    B, Hq, Hkv, N, T, d = _geometry(q, k, cu_seqlens, max_seqlen, batch)
+    B, Hq, Hkv, Nq, Tq, Nk, Tk, d, kv = _geometry_kv(q, k, cu_seqlens, max_seqlen, cu_seqlens_k,
+                                                     max_seqlen_k, batch)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty((T, Hq, d), dtype=out_dtype, device=q.device)
-    lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
-    ws_bytes = fa_fwd_workspace_size(B, Hq, N, T)
+    o = torch.empty((Tq, Hq, d), dtype=out_dtype, device=q.device)
+    lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    ws_bytes = fa_fwd_workspace_size(B, Hq, Nq, Tq)
     ws = workspace if workspace is not None else torch.empty(
         max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
-    _check(fa_fwd(q, k, v, o, out_dtype, lse, B, Hq, Hkv, N, T, d, scale, causal, cu_seqlens, ws,
-                  ws_bytes, stream), "fa_fwd")
+    if kv:
+        _check(fa_fwd_kv(q, k, v, o, out_dtype, lse, B, Hq, Hkv, Nq, Tq, Nk, Tk, d, scale, causal,
+                         cu_seqlens, cu_seqlens_k, ws, ws_bytes, stream), "fa_fwd_kv")
+    else:
+        _check(fa_fwd(q, k, v, o, out_dtype, lse, B, Hq, Hkv, Nq, Tq, d, scale, causal,
+                      cu_seqlens, ws, ws_bytes, stream), "fa_fwd")
     return o, lse
 
 
 def backward(q, k, v, o, dout, lse, causal=False, scale=None, cu_seqlens=None, max_seqlen=None,
              batch=None, deterministic=False, grad_dtype=torch.bfloat16, stream=None,
-             workspace=None, check_status=False):
+             workspace=None, check_status=False, cu_seqlens_k=None, max_seqlen_k=None):
     """Attention backward (preprocess + backward) through the C ABI; returns (dq, dk, dv)."""
-    B, Hq, Hkv, N, T, d = _geometry(q, k, cu_seqlens, max_seqlen, batch)
+    B, Hq, Hkv, Nq, Tq, Nk, Tk, d, kv = _geometry_kv(q, k, cu_seqlens, max_seqlen, cu_seqlens_k,
+                                                     max_seqlen_k, batch)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    dq = torch.empty((T, Hq, d), dtype=grad_dtype, device=q.device)
-    dk = torch.empty((T, Hkv, d), dtype=grad_dtype, device=q.device)
-    dv = torch.empty((T, Hkv, d), dtype=grad_dtype, device=q.device)
-    D = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
-    ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, N, T, d)
+    dq = torch.empty((Tq, Hq, d), dtype=grad_dtype, device=q.device)
+    dk = torch.empty((Tk, Hkv, d), dtype=grad_dtype, device=q.device)
+    dv = torch.empty((Tk, Hkv, d), dtype=grad_dtype, device=q.device)
+    D = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    if kv:
+        ws_bytes = fa_bwd_kv_workspace_size(B, Hq, Hkv, Nq, Tq, Nk, Tk, d)
+    else:
+        ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, Nq, Tq, d)
     ws = workspace if workspace is not None else torch.empty(
         max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
-    _check(fa_bwd_preprocess(o, o.dtype, dout, D, ws, ws_bytes, B, Hq, Hkv, N, T, d, causal,
-                             cu_seqlens, deterministic, stream), "fa_bwd_preprocess")
-    _check(fa_bwd(q, k, v, dout, lse, D, dq, dk, dv, grad_dtype, ws, ws_bytes, B, Hq, Hkv, N, T, d,
-                  scale, causal, cu_seqlens, deterministic, stream), "fa_bwd")
-    if check_status:
+    if kv:
+        _check(fa_bwd_kv_preprocess(o, o.dtype, dout, D, ws, ws_bytes, B, Hq, Hkv, Nq, Tq, Nk, Tk,
+                                    d, causal, cu_seqlens, cu_seqlens_k, deterministic, stream),
+               "fa_bwd_kv_preprocess")
+        _check(fa_bwd_kv(q, k, v, dout, lse, D, dq, dk, dv, grad_dtype, ws, ws_bytes, B, Hq, Hkv,
+                         Nq, Tq, Nk, Tk, d, scale, causal, cu_seqlens, cu_seqlens_k,
+                         deterministic, stream), "fa_bwd_kv")
+    else:
+        _check(fa_bwd_preprocess(o, o.dtype, dout, D, ws, ws_bytes, B, Hq, Hkv, Nq, Tq, d, causal,
+                                 cu_seqlens, deterministic, stream), "fa_bwd_preprocess")
+        _check(fa_bwd(q, k, v, dout, lse, D, dq, dk, dv, grad_dtype, ws, ws_bytes, B, Hq, Hkv, Nq,
+                      Tq, d, scale, causal, cu_seqlens, deterministic, stream), "fa_bwd")
+    if check_status and Tq > 0 and Tk > 0 and B > 0:
         _check(fa_check_device_status(ws, stream), "fa_bwd (device)")
     return dq, dk, dv
 
 
 class _Attention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, causal, scale, cu_seqlens, max_seqlen, batch, deterministic):
-        o, lse = forward(q, k, v, causal, scale, cu_seqlens, max_seqlen, batch)
-        ctx.save_for_backward(q, k, v, o, lse, cu_seqlens)
-        ctx.args = (causal, scale, max_seqlen, batch, deterministic)
+    def forward(ctx, q, k, v, causal, scale, cu_seqlens, max_seqlen, batch, deterministic,
+                cu_seqlens_k, max_seqlen_k):
+        o, lse = forward(q, k, v, causal, scale, cu_seqlens, max_seqlen, batch,
+                         cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k)
+        ctx.save_for_backward(q, k, v, o, lse, cu_seqlens, cu_seqlens_k)
+        ctx.args = (causal, scale, max_seqlen, batch, deterministic, max_seqlen_k)
         return o
 
     @staticmethod
     def backward(ctx, dout):
-        q, k, v, o, lse, cu_seqlens = ctx.saved_tensors
-        causal, scale, max_seqlen, batch, deterministic = ctx.args
+        q, k, v, o, lse, cu_seqlens, cu_seqlens_k = ctx.saved_tensors
+        causal, scale, max_seqlen, batch, deterministic, max_seqlen_k = ctx.args
         dq, dk, dv = backward(q, k, v, o, dout.contiguous(), lse, causal, scale, cu_seqlens,
-                              max_seqlen, batch, deterministic)
-        return dq, dk, dv, None, None, None, None, None, None
+                              max_seqlen, batch, deterministic, cu_seqlens_k=cu_seqlens_k,
+                              max_seqlen_k=max_seqlen_k)
+        return dq, dk, dv, None, None, None, None, None, None, None, None
 
 
 def attention(q, k, v, causal=False, scale=None, cu_seqlens=None, max_seqlen=None, batch=None,
-              deterministic=False):
+              deterministic=False, cu_seqlens_k=None, max_seqlen_k=None):
     """Differentiable attention (autograd wrapper around forward/backward)."""
-    return _Attention.apply(q, k, v, causal, scale, cu_seqlens, max_seqlen, batch, deterministic)
+    return _Attention.apply(q, k, v, causal, scale, cu_seqlens, max_seqlen, batch, deterministic,
+                            cu_seqlens_k, max_seqlen_k)

@@ -96,8 +96,13 @@ struct BwdSmem {
 };
 static_assert(sizeof(BwdSmem<128>) <= 232448, "backward shared memory exceeds 227 KB");
 
+// One work unit: key/value tile j of sequence b, query head h (key/value head
+// g).  t0/L are the query tokens, tk0/Lk the key/value tokens; under the
+// causal mask query row r sees key c iff c <= r + off, off = Lk - L.  nt =
+// query tiles, ntk = key/value tiles, i0 = first query tile with a row that
+// sees a key of tile j, ni = query tiles the unit visits.
 struct BUnit {
-    int b, j, h, g, t0, L, nt, ni;
+    int b, j, h, g, t0, L, tk0, Lk, off, nt, ntk, i0, ni;
 };
 
 __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
@@ -107,14 +112,18 @@ __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
     x.h = unit_head(u.y);
     x.g = (int)(((long long)x.h * p.Hkv) / p.Hq);
     seq_bounds(p.cu_seqlens, p.N, x.b, x.t0, x.L);
+    seq_bounds(p.cu_seqlens_k, p.Nk, x.b, x.tk0, x.Lk);
+    x.off = x.Lk - x.L;
     x.nt = cdiv(x.L, kTile);
-    x.ni = p.causal ? x.nt - x.j : x.nt;
+    x.ntk = cdiv(x.Lk, kTile);
+    x.i0 = p.causal ? max(0, floor_div(x.j * kTile - x.off, kTile)) : 0;
+    x.ni = max(0, x.nt - x.i0);  // 0 only when the sequence has no queries
     return x;
 }
 
 // Query tile visited at step s of unit x.
-//  - deterministic causal: i = j, j+1, ..., so unit j's contribution to tile i
-//    is the (i - j)-th and no unit waits on its first dQ write;
+//  - deterministic causal: i = i0, i0+1, ... (i0 = j for equal lengths), so
+//    unit j+1 reaches every tile one step before unit j;
 //  - deterministic non-causal and atomic non-causal: i = 0, 1, ...;
 //  - atomic causal: descending from the last tile.
 // In atomic mode every unit of a (sequence, head) walks the tiles in the same
@@ -122,14 +131,17 @@ __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
 // the same dQ tile while it is resident in L2.
 __device__ __forceinline__ int walk_tile(const BUnit& x, int s, int deterministic, int causal) {
     if (!causal) return s;
-    return deterministic ? x.j + s : x.nt - 1 - s;
+    return deterministic ? x.i0 + s : x.nt - 1 - s;
 }
 
 // Deterministic mode: how many contributions to dQ tile i precede unit x's.
-// Contributions arrive in descending key/value tile: under the causal mask
-// tile i receives them from units i, i-1, ..., 0; without it from n-1, ..., 0.
+// Contributions arrive in descending key/value tile: from jmax(i), ..., 0,
+// where jmax(i) is the last key/value tile a row of query tile i sees (i for
+// equal lengths under the causal mask; ntk - 1 without it).
 __device__ __forceinline__ int dq_rank(const BUnit& x, int i, int causal) {
-    return causal ? i - x.j : x.nt - 1 - x.j;
+    const int jmax = causal ? min(x.ntk - 1, floor_div((i + 1) * kTile + x.off - 1, kTile))
+                            : x.ntk - 1;
+    return jmax - x.j;
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* flag, WsHeader* hdr, int code) {
@@ -318,9 +330,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
                 for (int cb = 0; cb < Cfg::kBoxes; ++cb) {
                     tma_load_3d(smem_u32(sm.k) + cb * 16384, &p.tm_k, bar, cb * 64, x.g,
-                                x.t0 + x.j * kTile);
+                                x.tk0 + x.j * kTile);
                     tma_load_3d(smem_u32(sm.v) + cb * 16384, &p.tm_v, bar, cb * 64, x.g,
-                                x.t0 + x.j * kTile);
+                                x.tk0 + x.j * kTile);
                 }
             }
             ++unit_it;
@@ -436,7 +448,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (unit.x < 0) break;
                 const BUnit x = decode_bunit(unit, p);
                 if (!(ok = wait_or_abort(smem_u32(&sm.kv_full), unit_it & 1, abort_flag, hdr))) break;
-                if (!(ok = issue_s(cnt))) break;
+                if (x.ni > 0 && !(ok = issue_s(cnt))) break;
                 for (int s = 0; s < x.ni; ++s, ++cnt) {
                     const int st = cnt & 1;
                     const uint32_t qaddr = smem_u32(sm.q[st]);
@@ -587,14 +599,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ++sched_it;
             if (unit.x < 0) break;
             const BUnit x = decode_bunit(unit, p);
-            const int c = x.j * kTile + rk;  // key position within the sequence
+            const int c = x.j * kTile + rk;  // key position within its sequence
             for (int s = 0; s < x.ni; ++s, ++cnt) {
                 const int i = walk_tile(x, s, p.deterministic, p.causal);
                 const int st = cnt & 1;
                 // visible query columns of this key row: [lo, hi); the warp skips the
                 // mask when every row sees every column
-                const int lo = p.causal ? max(0, c - i * kTile) : 0;
-                const int hi = c < x.L ? min(kTile, x.L - i * kTile) : 0;
+                const int lo = p.causal ? max(0, c - x.off - i * kTile) : 0;
+                const int hi = c < x.Lk ? min(kTile, x.L - i * kTile) : 0;
                 const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kTile);
                 if (!(ok = warp_wait(smem_u32(&sm.q_full[st]), (cnt >> 1) & 1, abort_flag, hdr)))
                     break;
@@ -773,8 +785,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!(ok = wg_wait(smem_u32(&sm.dkv_full), unit_it & 1, abort_flag, hdr))) break;
             tc_fence_after();
             const int kr = x.j * kTile + rr;
-            const bool valid = kr < x.L;
-            const size_t tok = (size_t)x.t0 + (size_t)kr;
+            const bool valid = kr < x.Lk;
+            const size_t tok = (size_t)x.tk0 + (size_t)kr;
+            const bool none = x.ni == 0;  // no query: dK = dV = 0, TMEM was not written
             const bool gqa = p.Hq != p.Hkv;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
@@ -786,6 +799,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tmem_ld32(tmem + lane_off + col + cc * 32, v);
                     tmem_ld_wait();
                     if (!valid) continue;
+                    if (none) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    }
                     if (gqa) {
                         float* acc = (which == 0 ? dk_acc : dv_acc) + (tok * p.Hq + x.h) * D + cc * 32;
                         float4* d4 = reinterpret_cast<float4*>(acc);
@@ -909,12 +926,12 @@ template <int D, bool F32>
 __global__ void __launch_bounds__(256)
     bwd_postprocess_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq,
                            const float* __restrict__ dk_acc, const float* __restrict__ dv_acc,
-                           void* __restrict__ dk, void* __restrict__ dv, int T, int Hq, int Hkv,
-                           float scale) {
+                           void* __restrict__ dk, void* __restrict__ dv, int Tq, int Tk, int Hq,
+                           int Hkv, float scale) {
     pdl_begin();
     constexpr int V = D / 4;  // float4 groups per row
-    const long long nq = (long long)T * Hq * V;
-    const long long nkv = dk_acc ? (long long)T * Hkv * V : 0;
+    const long long nq = (long long)Tq * Hq * V;
+    const long long nkv = dk_acc ? (long long)Tk * Hkv * V : 0;
     const long long stride = (long long)gridDim.x * blockDim.x;
     const int grp = Hq / Hkv;
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nq + 2 * nkv;
@@ -964,7 +981,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, int num_sms, cudaStream_t stream) {
     const size_t smem = sizeof(BwdSmem<D>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long long bound = max_tiles(p.B, p.T, kTile) * p.Hq;
+    const long long bound = max_tiles(p.B, p.Tk, kTile) * p.Hq;  // units are key/value tiles
     const int grid = (int)(bound < num_sms ? bound : num_sms);
     if (grid <= 0) return cudaSuccess;
     return launch_pdl(kern, dim3(grid), dim3(kBwdThreads), smem, stream, p);
@@ -997,15 +1014,15 @@ cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const float* dk_acc,
-                                   const float* dv_acc, void* dk, void* dv, int T, int Hq,
-                                   int Hkv, int d, float scale, int grad_fp32, int num_sms,
-                                   cudaStream_t stream) {
-    const long long work = (long long)T * (Hq + (dk_acc ? 2 * Hkv : 0)) * d / 4;
+                                   const float* dv_acc, void* dk, void* dv, int Tq, int Tk,
+                                   int Hq, int Hkv, int d, float scale, int grad_fp32,
+                                   int num_sms, cudaStream_t stream) {
+    const long long work = ((long long)Tq * Hq + (dk_acc ? 2LL * Tk * Hkv : 0)) * d / 4;
     const int grid = grid_for(work, 256, num_sms);
     cudaError_t e;
 #define FA_POST(DD, FF)                                                                   \
     e = launch_pdl(bwd_postprocess_kernel<DD, FF>, dim3(grid), dim3(256), 0, stream, dq_acc, dq, \
-                   dk_acc, dv_acc, dk, dv, T, Hq, Hkv, scale)
+                   dk_acc, dv_acc, dk, dv, Tq, Tk, Hq, Hkv, scale)
     if (d == 128) {
         if (grad_fp32) FA_POST(128, true); else FA_POST(128, false);
     } else {

@@ -90,30 +90,43 @@ __host__ __device__ inline FwdWs fwd_ws_layout(int B, int Hq, int T) {
 
 // Backward workspace: header | unit list (int2) | per-sequence query-tile
 // offsets (int[B+1]) | semaphores (int[Hq * max_qtiles]) | dQ accumulator
-// fp32 [T,Hq,d] | (GQA only) dK and dV partials fp32 [T,Hq,d].
+// fp32 [Tq,Hq,d] | (GQA only) dK and dV partials fp32 [Tk,Hq,d].  Units are
+// key/value tiles (Tk tokens); dQ tiles and semaphores are query tiles (Tq).
 struct BwdWs {
     size_t units, tile_off, sems, dq_acc, dk_acc, dv_acc, bytes;
     long long max_units, max_qtiles;
 };
 
-__host__ __device__ inline BwdWs bwd_ws_layout(int B, int Hq, int Hkv, int T, int d) {
+__host__ __device__ inline BwdWs bwd_ws_layout(int B, int Hq, int Hkv, int Tq, int Tk, int d) {
     BwdWs w;
-    w.max_qtiles = max_tiles(B, T, kTile);
-    w.max_units = w.max_qtiles * (long long)Hq;
+    w.max_qtiles = max_tiles(B, Tq, kTile);
+    w.max_units = max_tiles(B, Tk, kTile) * (long long)Hq;
     w.units = kAlign;
     w.tile_off = align_up(w.units + (size_t)w.max_units * 8, kAlign);
     w.sems = align_up(w.tile_off + (size_t)(B + 1) * 4, kAlign);
     w.dq_acc = align_up(w.sems + (size_t)w.max_qtiles * (size_t)Hq * 4, kAlign);
-    size_t acc = (size_t)T * (size_t)Hq * (size_t)d * 4;
-    w.dk_acc = align_up(w.dq_acc + acc, kAlign);
+    const size_t acc_q = (size_t)Tq * (size_t)Hq * (size_t)d * 4;
+    const size_t acc_k = (size_t)Tk * (size_t)Hq * (size_t)d * 4;
+    w.dk_acc = align_up(w.dq_acc + acc_q, kAlign);
     if (Hq != Hkv) {
-        w.dv_acc = align_up(w.dk_acc + acc, kAlign);
-        w.bytes = align_up(w.dv_acc + acc, kAlign);
+        w.dv_acc = align_up(w.dk_acc + acc_k, kAlign);
+        w.bytes = align_up(w.dv_acc + acc_k, kAlign);
     } else {
         w.dv_acc = w.dk_acc;
         w.bytes = w.dk_acc;
     }
     return w;
+}
+
+__host__ __device__ inline BwdWs bwd_ws_layout(int B, int Hq, int Hkv, int T, int d) {
+    return bwd_ws_layout(B, Hq, Hkv, T, T, d);
+}
+
+// Causal mask with Lq queries and Lk keys: the queries are the last Lq
+// positions of the key sequence, so query row r sees key c iff c <= r + off,
+// off = Lk - Lq (0 for equal lengths).
+__host__ __device__ inline int floor_div(int a, int b) {
+    return a >= 0 ? a / b : -((-a + b - 1) / b);
 }
 
 // Sequence geometry: start token and length of sequence b.

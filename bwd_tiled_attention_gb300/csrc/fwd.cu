@@ -6,7 +6,10 @@
 // output O~ that is rescaled when m grows, and one division by l at the end;
 // only LSE = m + log l is stored.  Key/value tiles entirely above the causal
 // diagonal are never visited; only tiles that straddle it (or the ragged end
-// of a sequence) are masked.
+// of a sequence) are masked.  Queries and keys may differ in length: the
+// queries are then the last positions of the key sequence (query row r sees
+// key c iff c <= r + Lk - Lq under the causal mask), and a row that sees no
+// key gets O = 0 and LSE = -inf.
 //
 // Blackwell design ("FlashAttention-4 wird offiziell veröffentlicht", section
 // "Neue Hardwaremerkmale von Blackwell": single-thread tcgen05.mma accumulating
@@ -72,8 +75,12 @@ struct FwdSmem {
     int zero;
 };
 
+// One work unit: query rows [256m, 256m + 256) of sequence b, head h.  t0/L
+// are the query tokens, tk0/Lk the key/value tokens; under the causal mask
+// query row r sees key c iff c <= r + Lk - L.  n[t] = key/value tiles query
+// tile t visits (0 when the tile is past the end, or sees no key at all).
 struct UnitGeom {
-    int b, m, h, g, t0, L, n[2], nkv;
+    int b, m, h, g, t0, L, tk0, Lk, n[2], nkv;
 };
 
 __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
@@ -83,6 +90,7 @@ __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
     x.h = unit_head(u.y);
     x.g = (int)(((long long)x.h * p.Hkv) / p.Hq);
     seq_bounds(p.cu_seqlens, p.N, x.b, x.t0, x.L);
+    seq_bounds(p.cu_seqlens_k, p.Nk, x.b, x.tk0, x.Lk);
     const int r0 = x.m * kFwdBlockRows;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -91,9 +99,9 @@ __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
             x.n[t] = 0;
         } else if (p.causal) {
             const int re = min(rs + kTile, x.L);  // one past last valid row
-            x.n[t] = cdiv(re, kTile);
+            x.n[t] = cdiv(max(re + x.Lk - x.L, 0), kTile);
         } else {
-            x.n[t] = cdiv(x.L, kTile);
+            x.n[t] = cdiv(x.Lk, kTile);
         }
     }
     x.nkv = max(x.n[0], x.n[1]);
@@ -135,6 +143,20 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* flag,
                                           WsHeader* hdr) {
     return __all_sync(0xffffffffu, wait_or_abort(bar, parity, flag, hdr));
+}
+
+// A query row that sees no key: O = 0, LSE = -inf.
+template <int D, bool OUT_FP32>
+__device__ __forceinline__ void write_keyless_row(const FwdParams& p, int h, size_t tok) {
+    p.lse[(size_t)h * p.T + tok] = -INFINITY;
+    const size_t base = (tok * p.Hq + h) * D;
+    if (OUT_FP32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base);
+        for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + base);
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
 }
 
 template <int D, bool OUT_FP32>
@@ -213,8 +235,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const int row0 = x.t0 + x.m * kFwdBlockRows;
                 if (!(ok = wait_or_abort(smem_u32(&sm.q_empty), (unit_it & 1) ^ 1, abort_flag, hdr)))
                     break;
+                // only the query tiles that see a key are loaded (none when no row of
+                // the unit sees one: the barrier then completes on the arrival alone)
                 const uint32_t qbar = smem_u32(&sm.q_full);
-                mbar_arrive_expect_tx(qbar, (x.n[1] > 0 ? 2 : 1) * Cfg::kTileBytes);
+                mbar_arrive_expect_tx(qbar, ((x.n[0] > 0) + (x.n[1] > 0)) * Cfg::kTileBytes);
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (x.n[t] == 0) continue;
@@ -232,11 +256,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     mbar_arrive_expect_tx(kb, Cfg::kTileBytes);
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_3d(smem_u32(sm.k[st]) + c * 16384, &p.tm_k, kb, c * 64, x.g,
-                                    x.t0 + j * kTile);
+                                    x.tk0 + j * kTile);
                     mbar_arrive_expect_tx(vb, Cfg::kTileBytes);
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_3d(smem_u32(sm.v[st]) + c * 16384, &p.tm_v, vb, c * 64, x.g,
-                                    x.t0 + j * kTile);
+                                    x.tk0 + j * kTile);
                     ++kv_it;
                 }
             }
@@ -324,6 +348,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     ++kv_it;
                 }
                 if (!ok) break;
+                if (x.nkv == 0) mma_commit(smem_u32(&sm.q_empty));  // no key: Q was not loaded
                 ++unit_it;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) ep[t] += x.n[t] > 0;
@@ -355,9 +380,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (unit.x < 0) break;
             const UnitGeom x = decode_unit(unit, p);
             const int nt = t == 0 ? x.n[0] : x.n[1];
-            if (nt == 0) continue;
             const int r = x.m * kFwdBlockRows + t * kTile + row;  // row within the sequence
-            const int limit = p.causal ? min(r + 1, x.L) : x.L;   // visible keys: col < limit
+            if (nt == 0) {
+                // the tile is past the end, or none of its rows sees a key (more
+                // queries than keys): O = 0 and LSE = -inf, nothing on chip
+                if (r < x.L) write_keyless_row<D, OUT_FP32>(p, x.h, (size_t)x.t0 + (size_t)r);
+                continue;
+            }
+            // visible keys: col < limit (end-aligned causal mask)
+            const int limit = p.causal ? min(r + 1 + x.Lk - x.L, x.Lk) : x.Lk;
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < nt; ++j) {
                 if (!(ok = warp_wait(smem_u32(&sm.s_full[t]), it & 1, abort_flag, hdr))) break;
@@ -449,7 +480,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!(ok = warp_wait(smem_u32(&sm.o_done[t]), (it - 1) & 1, abort_flag, hdr))) break;
             tc_fence_after();
             const bool valid = r < x.L;
-            const float inv_l = 1.f / l;
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;  // l = 0: the row sees no key
             const size_t tok = (size_t)x.t0 + (size_t)r;
             if (valid) p.lse[(size_t)x.h * p.T + tok] = (m_ref + __log2f(l)) * 0.69314718055994531f;
 #pragma unroll 1

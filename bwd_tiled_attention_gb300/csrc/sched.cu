@@ -12,7 +12,11 @@
 // tile count (descending, ties by index), and writes the ordered list of work
 // units (sequence, tile, head) into the workspace, heads innermost.  The
 // attention kernels take units from that list through an atomic counter that
-// this kernel resets, so CTAs that finish early pick up the next unit.
+// this kernel resets, so CTAs that finish early pick up the next unit.  The
+// backward's units are key/value tiles while its dQ semaphores are per query
+// tile, so it also passes the query boundaries, from which this kernel writes
+// the per-sequence query-tile offsets; both sides' lengths are checked against
+// their bounds.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -23,13 +27,16 @@ namespace fa {
 constexpr int kSchedThreads = 1024;
 
 struct SchedArgs {
-    const int* cu_seqlens;  // device int32[B+1] or null (dense)
+    const int* cu_seqlens;  // device int32[B+1] or null (dense): the unit tiles
+    const int* cu_aux;      // the other side's boundaries (null when dense)
     int B, N, H, rows;      // rows per tile
+    int T;                  // tokens on the unit side (cu_seqlens[B] must equal it)
+    int N_aux, T_aux;       // bound on the other side's lengths, its tokens
     int order;              // SchedOrder
     int max_units;          // capacity of the unit list
     WsHeader* header;
     int2* units;
-    int* tile_off;          // int[B+1] per-sequence tile offsets (may be null)
+    int* tile_off;          // int[B+1] offsets of the other side's tiles (may be null)
 };
 
 // Number of sequences whose tile count exceeds m, given counts sorted descending.
@@ -63,13 +70,14 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedArgs a) {
     if (a.cu_seqlens == nullptr) {
         // Dense batch: every sequence has nt tiles; closed-form order.
         const int nt = cdiv(a.N, a.rows);
+        const int nt_aux = cdiv(a.N_aux, a.rows);
         const long long per_level = (long long)B * H;
         const long long total = per_level * nt;
         if (tid == 0) {
             a.header->n_units = (int)(total <= a.max_units ? total : 0);
             a.header->counter = 0;
             a.header->error = total <= a.max_units ? 0 : kErrSchedule;
-            a.header->n_qtiles = B * nt;
+            a.header->n_qtiles = B * nt_aux;
         }
         if (total > a.max_units) return;
         for (long long u = tid; u < total; u += kSchedThreads) {
@@ -89,7 +97,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedArgs a) {
             a.units[u] = make_int2(b, make_unit_y(tile, h));
         }
         if (a.tile_off)
-            for (int b = tid; b <= B; b += kSchedThreads) a.tile_off[b] = b * nt;
+            for (int b = tid; b <= B; b += kSchedThreads) a.tile_off[b] = b * nt_aux;
         return;
     }
 
@@ -99,11 +107,20 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedArgs a) {
     int* nt_sorted = sorted + B;                       // [B] tile count at rank r
     long long* prefix = reinterpret_cast<long long*>(  // [max(B, maxnt) + 1]
         sm + align_up((size_t)3 * B * sizeof(int), 16));
-    if (tid == 0) { s_maxnt = 0; s_bad = 0; }
+    if (tid == 0) {
+        s_maxnt = 0;
+        // the boundaries must span exactly the tokens the buffers hold
+        s_bad = a.cu_seqlens[0] != 0 || a.cu_seqlens[B] != a.T ||
+                (a.cu_aux && (a.cu_aux[0] != 0 || a.cu_aux[B] != a.T_aux));
+    }
     __syncthreads();
     for (int b = tid; b < B; b += kSchedThreads) {
         const int L = a.cu_seqlens[b + 1] - a.cu_seqlens[b];
         if (L < 0 || L > a.N) atomicOr(&s_bad, 1);  // N bounds every length
+        if (a.cu_aux) {
+            const int La = a.cu_aux[b + 1] - a.cu_aux[b];
+            if (La < 0 || La > a.N_aux) atomicOr(&s_bad, 1);
+        }
         const int nt = L > 0 ? cdiv(L, a.rows) : 0;
         nt_of[b] = nt;
         atomicMax(&s_maxnt, nt);
@@ -161,7 +178,10 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(SchedArgs a) {
     }
     if (a.tile_off && tid == 0) {
         int acc = 0;
-        for (int b = 0; b < B; ++b) { a.tile_off[b] = acc; acc += nt_of[b]; }
+        for (int b = 0; b < B; ++b) {
+            a.tile_off[b] = acc;
+            acc += cdiv(a.cu_aux[b + 1] - a.cu_aux[b], a.rows);
+        }
         a.tile_off[B] = acc;
         a.header->n_qtiles = acc;
     } else if (tid == 0) {
@@ -191,11 +211,16 @@ size_t sched_smem_bytes(int B, int maxnt_bound) {
     return align_up((size_t)3 * B * sizeof(int), 16) + (size_t)slots * sizeof(long long);
 }
 
-cudaError_t launch_sched(const int* cu_seqlens, int B, int N, int H, int rows, int order,
+cudaError_t launch_sched(const int* cu_seqlens, int B, int N, int T, int H, int rows, int order,
                          long long max_units, void* workspace, size_t units_off,
-                         size_t tile_off_off, bool want_tile_off, cudaStream_t stream) {
+                         size_t tile_off_off, bool want_tile_off, const int* cu_tiles_seqlens,
+                         int N_tiles, int T_tiles, cudaStream_t stream) {
     SchedArgs a;
     a.cu_seqlens = cu_seqlens;
+    a.cu_aux = cu_tiles_seqlens;
+    a.T = T;
+    a.N_aux = N_tiles;
+    a.T_aux = T_tiles;
     a.B = B;
     a.N = N;
     a.H = H;

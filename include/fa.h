@@ -34,8 +34,9 @@
  * - Query head h uses key/value head floor(h * Hkv / Hq); Hq % Hkv == 0.
  * - d must be 64 or 128.  Inputs are bf16.  scale multiplies QK^T (usually
  *   1/sqrt(d)) and must be positive.  causal = 1 hides key j from query i
- *   when j > i (positions within the sequence, top-left aligned; queries and
- *   keys have equal length).
+ *   when j > i (positions within the sequence; queries and keys have equal
+ *   length).  The *_kv calls take separate query and key/value lengths; their
+ *   causal mask is described at fa_fwd_kv.
  * - Every call is asynchronous on `stream` (NULL = the legacy default stream)
  *   and never synchronises, except fa_check_device_status.  The return value
  *   reports argument validation and launch errors only; it never aborts.
@@ -98,6 +99,31 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fa_dtype 
                  fa_stream_t stream);
 
 /*
+ * Forward with different query and key/value lengths (new tokens attending
+ * to a cache of earlier ones, or cross-attention).  The pages state the
+ * causal mask only for equal lengths; here the Lq queries of a sequence are
+ * taken to be the LAST Lq positions of its Lk keys, so with causal = 1 query
+ * i (0-based within its sequence) sees key j iff j <= i + (Lk - Lq).  For
+ * Lq = Lk this is the mask of fa_fwd.  A row that sees no key (causal with
+ * i < Lq - Lk, or Lk = 0) gets O = 0 and LSE = -inf.
+ *   q, o [Tq,Hq,d], lse [Hq,Tq]; k, v [Tk,Hkv,d].  Other arguments as in fa_fwd.
+ *   Dense batch: cu_seqlens_q = cu_seqlens_k = NULL, query sequence b owns
+ *   tokens [b*Nq, (b+1)*Nq) and its keys [b*Nk, (b+1)*Nk); Tq = B*Nq and
+ *   Tk = B*Nk (total_q / total_k 0 or equal to those).  Packed batch: both
+ *   cu_seqlens_q and cu_seqlens_k (device int32[B+1] each) with total_q =
+ *   cu_seqlens_q[B], total_k = cu_seqlens_k[B], and Nq, Nk bounds on every
+ *   query and key length (a longer one is reported as FA_ERR_INVALID_ARG by
+ *   fa_check_device_status and produces no output).  Passing only one of the
+ *   two is FA_ERR_INVALID_ARG.
+ *   workspace: >= fa_fwd_workspace_size(B, Hq, Nq, total_q) bytes.
+ */
+fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype,
+                    float* lse, int B, int Hq, int Hkv, int Nq, int total_q, int Nk, int total_k,
+                    int d, float scale, int causal, const int* cu_seqlens_q,
+                    const int* cu_seqlens_k, void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream);
+
+/*
  * Workspace of the backward pass (fa_bwd_preprocess + fa_bwd), in bytes: a
  * header (device error word, work counter), the scheduler's ordered unit list
  * and per-sequence tile offsets, one semaphore per (query head, query tile)
@@ -151,6 +177,36 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout, 
                  void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N,
                  int total_tokens, int d, float scale, int causal, const int* cu_seqlens,
                  int deterministic, fa_stream_t stream);
+
+/*
+ * Backward with different query and key/value lengths, the gradient of
+ * fa_fwd_kv: the same three steps with the query/key geometry of fa_fwd_kv.
+ *   fa_bwd_kv_workspace_size: bytes of the workspace (the dQ accumulator and
+ *   semaphores cover the Tq query tokens, the unit list and the GQA dK/dV
+ *   partials the Tk key tokens).
+ *   fa_bwd_kv_preprocess: D [Hq,Tq] and the workspace reset, as
+ *   fa_bwd_preprocess; o, dout [Tq,Hq,d].
+ *   fa_bwd_kv: dq [Tq,Hq,d], dk/dv [Tk,Hkv,d]; q, dout [Tq,Hq,d], k, v
+ *   [Tk,Hkv,d], lse and D [Hq,Tq].  Keys that no query sees get dK = dV = 0;
+ *   rows that see no key get dQ = 0.  deterministic = 1 gives bit-identical
+ *   results across runs as for fa_bwd.
+ * Arguments, errors and ownership otherwise as fa_bwd_preprocess / fa_bwd.
+ */
+size_t fa_bwd_kv_workspace_size(int B, int Hq, int Hkv, int Nq, int total_q, int Nk,
+                                int total_k, int d);
+
+fa_status fa_bwd_kv_preprocess(const void* o, fa_dtype o_dtype, const void* dout, float* D,
+                               void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                               int Nq, int total_q, int Nk, int total_k, int d, int causal,
+                               const int* cu_seqlens_q, const int* cu_seqlens_k,
+                               int deterministic, fa_stream_t stream);
+
+fa_status fa_bwd_kv(const void* q, const void* k, const void* v, const void* dout,
+                    const float* lse, const float* D, void* dq, void* dk, void* dv,
+                    fa_dtype grad_dtype, void* workspace, size_t workspace_bytes, int B, int Hq,
+                    int Hkv, int Nq, int total_q, int Nk, int total_k, int d, float scale,
+                    int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                    int deterministic, fa_stream_t stream);
 
 /*
  * Backward pass for callers that cannot allocate device memory: same inputs,

@@ -11,7 +11,9 @@ only), then Q, K, V, dO with ``randn`` in float32 at the packed shape
 
 The named workloads are the shapes the tiled-attention pages discuss (dense
 mid-size batches, one long causal sequence, grouped/multi-query heads, and a
-packed variable-length batch) at head dimension 64 or 128.
+packed variable-length batch) at head dimension 64 or 128.  ``make_inputs_kv``
+draws queries and keys of different lengths (new tokens against a longer key
+sequence): Q and dO over the query tokens, K and V over the key tokens.
 """
 from __future__ import annotations
 
@@ -114,3 +116,42 @@ def make_workload(w: Workload, **override):
         kw.pop("len_range", None)
         kw.pop("lengths", None)
     return make_inputs(**kw)
+
+
+def make_inputs_kv(Hq, Hkv, d, seed, lengths_q, lengths_k, qk_scale=1.0):
+    """Draw (q, k, v, dout, cu_seqlens, cu_seqlens_k, lengths, lengths_k) as bf16
+    CPU tensors with separate query and key/value lengths per sequence.
+    q, dout: [Tq, Hq, d]; k, v: [Tk, Hkv, d]; draw order Q, K, V, dO."""
+    gen = torch.Generator().manual_seed(int(seed))
+    lengths_q = [int(x) for x in lengths_q]
+    lengths_k = [int(x) for x in lengths_k]
+    assert len(lengths_q) == len(lengths_k)
+    Tq, Tk = sum(lengths_q), sum(lengths_k)
+    q = torch.randn((Tq, Hq, d), generator=gen, dtype=torch.float32)
+    k = torch.randn((Tk, Hkv, d), generator=gen, dtype=torch.float32)
+    v = torch.randn((Tk, Hkv, d), generator=gen, dtype=torch.float32)
+    dout = torch.randn((Tq, Hq, d), generator=gen, dtype=torch.float32)
+    if qk_scale != 1.0:
+        q = q * qk_scale
+        k = k * qk_scale
+    return dict(
+        q=q.to(torch.bfloat16), k=k.to(torch.bfloat16), v=v.to(torch.bfloat16),
+        dout=dout.to(torch.bfloat16), cu_seqlens=cu_from_lengths(lengths_q),
+        cu_seqlens_k=cu_from_lengths(lengths_k), lengths=lengths_q, lengths_k=lengths_k)
+
+
+def kv_workloads() -> dict:
+    """Named workloads with different query and key lengths: (B, Hq, Hkv, d,
+    causal, seed, lengths_q, lengths_k).  ``chunk_causal``: 2048 new tokens per
+    sequence against 8192 keys (6144 earlier positions plus the new ones);
+    ``varlen_chunks``: packed sequences whose key length is the query length
+    plus a drawn number of earlier positions."""
+    gen = torch.Generator().manual_seed(9)
+    lq = [int(x) for x in torch.randint(1, 2049, (8,), generator=gen)]
+    extra = [int(x) for x in torch.randint(0, 6145, (8,), generator=gen)]
+    return {
+        "chunk_causal": dict(B=4, Hq=16, Hkv=16, d=128, causal=True, seed=5,
+                             lengths_q=[2048] * 4, lengths_k=[8192] * 4),
+        "varlen_chunks": dict(B=8, Hq=16, Hkv=4, d=128, causal=True, seed=6, lengths_q=lq,
+                              lengths_k=[a + b for a, b in zip(lq, extra)]),
+    }

@@ -116,6 +116,49 @@ def test_bwd_rejects_bad_arguments(L):
     assert fa.fa_bwd_preprocess(**dict(pre, o_dtype=9)) == fa.FA_ERR_INVALID_ARG
 
 
+def fwd_kv_call(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, o_dtype=fa.FA_BF16, lse=FAKE, B=2, Hq=4, Hkv=2,
+                Nq=64, total_q=0, Nk=200, total_k=0, d=128, scale=0.125, causal=1,
+                cu_seqlens_q=None, cu_seqlens_k=None, workspace=FAKE, workspace_bytes=1 << 20,
+                stream=0)
+    args.update(kw)
+    return fa.fa_fwd_kv(**args)
+
+
+def test_kv_calls_reject_bad_arguments(L):
+    # queries and keys are both dense or both packed
+    assert fwd_kv_call(cu_seqlens_q=FAKE, total_q=10) == fa.FA_ERR_INVALID_ARG
+    assert fwd_kv_call(cu_seqlens_k=FAKE, total_k=10) == fa.FA_ERR_INVALID_ARG
+    assert fwd_kv_call(total_k=300) == fa.FA_ERR_INVALID_ARG    # dense Tk must be B*Nk
+    assert fwd_kv_call(Nk=-1) == fa.FA_ERR_INVALID_ARG
+    assert fwd_kv_call(d=256) == fa.FA_ERR_UNSUPPORTED
+    assert fwd_kv_call(k=FAKE + 8) == fa.FA_ERR_INVALID_ARG
+    assert fwd_kv_call(Nq=0) == fa.FA_OK                        # no queries: nothing to do
+    pre = dict(o=FAKE, o_dtype=fa.FA_BF16, dout=FAKE, D=FAKE, workspace=FAKE,
+               workspace_bytes=1 << 30, B=2, Hq=4, Hkv=2, Nq=64, total_q=0, Nk=200, total_k=0,
+               d=128, causal=1, cu_seqlens_q=None, cu_seqlens_k=FAKE, deterministic=0, stream=0)
+    assert fa.fa_bwd_kv_preprocess(**pre) == fa.FA_ERR_INVALID_ARG
+    bwd = dict(q=FAKE, k=FAKE, v=FAKE, dout=FAKE, lse=FAKE, D=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+               grad_dtype=fa.FA_BF16, workspace=FAKE, workspace_bytes=64, B=2, Hq=4, Hkv=2,
+               Nq=64, total_q=0, Nk=200, total_k=0, d=128, scale=0.1, causal=1,
+               cu_seqlens_q=None, cu_seqlens_k=None, deterministic=0, stream=0)
+    assert fa.fa_bwd_kv(**bwd) == fa.FA_ERR_INVALID_ARG          # workspace too small
+    assert fa.fa_bwd_kv(**dict(bwd, Hkv=3)) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_kv(**dict(bwd, B=0)) == fa.FA_OK
+
+
+def test_kv_workspace_sizes(L):
+    Hq, d = 8, 128
+    # equal lengths: the same bytes as the equal-length call
+    assert fa.fa_bwd_kv_workspace_size(2, Hq, 2, 300, 0, 300, 0, d) == \
+        fa.fa_bwd_workspace_size(2, Hq, 2, 300, 0, d)
+    # the dQ accumulator covers the queries, the GQA dK/dV partials the keys
+    small_k = fa.fa_bwd_kv_workspace_size(2, Hq, 2, 1024, 0, 128, 0, d)
+    big_k = fa.fa_bwd_kv_workspace_size(2, Hq, 2, 1024, 0, 4096, 0, d)
+    assert big_k - small_k >= 2 * 2 * (4096 - 128) * Hq * d * 4
+    assert small_k >= 2 * 1024 * Hq * d * 4
+
+
 def test_check_status_null(L):
     assert fa.fa_check_device_status(None, 0) == fa.FA_ERR_INVALID_ARG
 
