@@ -4,7 +4,10 @@ One step = forward (fa_fwd) + backward (fa_bwd_preprocess + fa_bwd) of the
 whole workload, with inputs resident in HBM and the L2 flushed before every
 step (a 512 MB write outside the step's events).  Throughput counts the
 algorithmic FLOPs 4*B*Hq*N^2*d (forward) and 2.5x that (backward), halved for
-causal; a packed variable-length batch uses sum(L_b^2) for B*N^2.
+causal; a packed variable-length batch uses sum(L_b^2) for B*N^2.  Workloads
+with different query and key lengths (fa_fwd_kv / fa_bwd_kv, the causal mask
+aligned at the end of the keys) count Lq*Lk per sequence, minus the hidden
+triangle Lq^2/2 under the causal mask (Lk^2/2 when Lq > Lk).
 
 Default workload: B=4, Hq=Hkv=16, N=2048, d=128, causal, bf16, seeded N(0,1)
 inputs (the mid-size dense configuration, causal).
@@ -42,11 +45,20 @@ FA_BWD_DRAM_BYTES = {"mid_causal": 773.8e6}
 NOMINAL_PEAK_TFLOPS = 2250.0
 
 
-def workload_flops(w, lengths):
-    sq = sum(L * L for L in lengths)
-    fwd = 4.0 * w.Hq * sq * w.d
-    if w.causal:
-        fwd /= 2.0
+def workload_flops(w, lengths, lengths_k=None):
+    if lengths_k is None:
+        sq = sum(L * L for L in lengths)
+        fwd = 4.0 * w.Hq * sq * w.d
+        if w.causal:
+            fwd /= 2.0
+        return fwd, 2.5 * fwd
+    pairs = 0.0
+    for lq, lk in zip(lengths, lengths_k):
+        if not w.causal:
+            pairs += lq * lk
+        else:
+            pairs += lq * lk - lq * lq / 2.0 if lq <= lk else lk * lk / 2.0
+    fwd = 4.0 * w.Hq * pairs * w.d
     return fwd, 2.5 * fwd
 
 
@@ -152,17 +164,20 @@ def cpu_baseline(w, inp, budget_s=12.0):
 
     q, k, v, do = (f64(inp[x]) for x in ("q", "k", "v", "dout"))
     cu = inp["cu_seqlens"].numpy()
+    cu_k = inp["cu_seqlens_k"].numpy() if "cu_seqlens_k" in inp else cu
     lengths = inp["lengths"]
     done_flops, heads = 0.0, 0
     grp = w.Hq // w.Hkv
     t0 = time.perf_counter()
     for b in range(len(lengths)):
         s0, s1 = int(cu[b]), int(cu[b + 1])
+        k0, k1 = int(cu_k[b]), int(cu_k[b + 1])
         for h in range(w.Hq):
             g = h // grp
-            oracle.attention(q[s0:s1, h:h + 1], k[s0:s1, g:g + 1], v[s0:s1, g:g + 1],
-                             [0, s1 - s0], w.scale, w.causal, dout=do[s0:s1, h:h + 1])
-            f, bw = workload_flops(w, [s1 - s0])
+            oracle.attention(q[s0:s1, h:h + 1], k[k0:k1, g:g + 1], v[k0:k1, g:g + 1],
+                             [0, s1 - s0], w.scale, w.causal, dout=do[s0:s1, h:h + 1],
+                             cu_seqlens_k=[0, k1 - k0])
+            f, bw = workload_flops(w, [s1 - s0], None if w.lengths_k is None else [k1 - k0])
             done_flops += (f + bw) / w.Hq
             heads += 1
             if time.perf_counter() - t0 >= budget_s:
@@ -178,8 +193,9 @@ def cpu_baseline(w, inp, budget_s=12.0):
 
 def config_of(w, inp, world):
     lengths = inp["lengths"]
+    nk = f" Nk={max(inp['lengths_k'])} (queries end-aligned)" if "lengths_k" in inp else ""
     return {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} "
-                        f"N={max(lengths)} d={w.d} {'causal' if w.causal else 'non-causal'}"
+                        f"N={max(lengths)}{nk} d={w.d} {'causal' if w.causal else 'non-causal'}"
                         f"{' deterministic' if w.deterministic else ''}",
             "global_batch": w.B * world, "seq_len": max(lengths), "tokens": sum(lengths) * world,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -198,7 +214,7 @@ def run_reference(args, w, inp, rank, world):
         vals.append(cpu_baseline(w, inp, budget_s=args.ref_step_s))
     wall = time.perf_counter() - t0
     value = statistics.mean(v["value"] for v in vals)
-    flops_step = sum(workload_flops(w, inp["lengths"]))
+    flops_step = sum(workload_flops(w, inp["lengths"], inp.get("lengths_k")))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": W,
@@ -249,12 +265,16 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     lengths = inp["lengths"]
+    lengths_k = inp.get("lengths_k")          # None: keys as long as the queries
+    kv = lengths_k is not None
     B, Hq, Hkv, d = w.B, w.Hq, w.Hkv, w.d
     N, T = max(lengths), sum(lengths)
+    Nk, Tk = (max(lengths_k), sum(lengths_k)) if kv else (N, T)
     scale = w.scale
-    varlen = w.len_range is not None
+    varlen = w.len_range is not None or len(set(lengths)) > 1 or (kv and len(set(lengths_k)) > 1)
     x = {k: inp[k].to(dev) for k in ("q", "k", "v", "dout")}
     cu = inp["cu_seqlens"].to(dev) if varlen else None
+    cu_k = inp["cu_seqlens_k"].to(dev) if (varlen and kv) else None
     o = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
     Dv = torch.empty((Hq, T), dtype=torch.float32, device=dev)
@@ -262,7 +282,8 @@ def main():
     dk = torch.empty_like(x["k"])
     dv = torch.empty_like(x["v"])
     fws_b = fa.fa_fwd_workspace_size(B, Hq, N, T)
-    bws_b = fa.fa_bwd_workspace_size(B, Hq, Hkv, N, T, d)
+    bws_b = (fa.fa_bwd_kv_workspace_size(B, Hq, Hkv, N, T, Nk, Tk, d) if kv
+             else fa.fa_bwd_workspace_size(B, Hq, Hkv, N, T, d))
     fws = torch.empty(fws_b, dtype=torch.uint8, device=dev)
     bws = torch.empty(bws_b, dtype=torch.uint8, device=dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -278,17 +299,31 @@ def main():
         gq, gk, gv = (dq, dk, dv) if grads is None else grads
         if events:
             events[0].record(stream)
-        check(fa.fa_fwd(xi["q"], xi["k"], xi["v"], o, fa.FA_BF16, lse, B, Hq, Hkv, N, T, d, scale,
-                        w.causal, cu, fws, fws_b, stream), "fa_fwd")
+        if kv:
+            check(fa.fa_fwd_kv(xi["q"], xi["k"], xi["v"], o, fa.FA_BF16, lse, B, Hq, Hkv, N, T, Nk,
+                               Tk, d, scale, w.causal, cu, cu_k, fws, fws_b, stream), "fa_fwd_kv")
+        else:
+            check(fa.fa_fwd(xi["q"], xi["k"], xi["v"], o, fa.FA_BF16, lse, B, Hq, Hkv, N, T, d,
+                            scale, w.causal, cu, fws, fws_b, stream), "fa_fwd")
         if events:
             events[1].record(stream)
-        check(fa.fa_bwd_preprocess(o, fa.FA_BF16, xi["dout"], Dv, bws, bws_b, B, Hq, Hkv, N, T, d,
-                                   w.causal, cu, det, stream), "fa_bwd_preprocess")
+        if kv:
+            check(fa.fa_bwd_kv_preprocess(o, fa.FA_BF16, xi["dout"], Dv, bws, bws_b, B, Hq, Hkv, N,
+                                          T, Nk, Tk, d, w.causal, cu, cu_k, det, stream),
+                  "fa_bwd_kv_preprocess")
+        else:
+            check(fa.fa_bwd_preprocess(o, fa.FA_BF16, xi["dout"], Dv, bws, bws_b, B, Hq, Hkv, N, T,
+                                       d, w.causal, cu, det, stream), "fa_bwd_preprocess")
         if events:
             events[2].record(stream)
-        check(fa.fa_bwd(xi["q"], xi["k"], xi["v"], xi["dout"], lse, Dv, gq, gk, gv, fa.FA_BF16,
-                        bws, bws_b, B, Hq, Hkv, N, T, d, scale, w.causal, cu, det, stream),
-              "fa_bwd")
+        if kv:
+            check(fa.fa_bwd_kv(xi["q"], xi["k"], xi["v"], xi["dout"], lse, Dv, gq, gk, gv,
+                               fa.FA_BF16, bws, bws_b, B, Hq, Hkv, N, T, Nk, Tk, d, scale,
+                               w.causal, cu, cu_k, det, stream), "fa_bwd_kv")
+        else:
+            check(fa.fa_bwd(xi["q"], xi["k"], xi["v"], xi["dout"], lse, Dv, gq, gk, gv,
+                            fa.FA_BF16, bws, bws_b, B, Hq, Hkv, N, T, d, scale, w.causal, cu, det,
+                            stream), "fa_bwd")
         if events:
             events[3].record(stream)
 
@@ -319,7 +354,7 @@ def main():
     t_pre = [e[1].elapsed_time(e[2]) for e in evs]
     t_bwd = [e[2].elapsed_time(e[3]) for e in evs]
     t_step = [e[0].elapsed_time(e[3]) for e in evs]
-    fl_f, fl_b = workload_flops(w, lengths)
+    fl_f, fl_b = workload_flops(w, lengths, lengths_k)
     value, total_ms = job_throughput((fl_f + fl_b) * K, sum(t_step), dist, dev)
     ms_per_step = total_ms / K
 

@@ -105,6 +105,9 @@ struct BUnit {
     int b, j, h, g, t0, L, tk0, Lk, off, nt, ntk, i0, ni;
 };
 
+// KV = false: keys and queries share their boundaries (Lk = L, off = 0), and
+// the geometry is the plain square one.
+template <bool KV>
 __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
     BUnit x;
     x.b = u.x;
@@ -112,12 +115,21 @@ __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
     x.h = unit_head(u.y);
     x.g = (int)(((long long)x.h * p.Hkv) / p.Hq);
     seq_bounds(p.cu_seqlens, p.N, x.b, x.t0, x.L);
-    seq_bounds(p.cu_seqlens_k, p.Nk, x.b, x.tk0, x.Lk);
-    x.off = x.Lk - x.L;
     x.nt = cdiv(x.L, kTile);
-    x.ntk = cdiv(x.Lk, kTile);
-    x.i0 = p.causal ? max(0, floor_div(x.j * kTile - x.off, kTile)) : 0;
-    x.ni = max(0, x.nt - x.i0);  // 0 only when the sequence has no queries
+    if constexpr (KV) {
+        seq_bounds(p.cu_seqlens_k, p.Nk, x.b, x.tk0, x.Lk);
+        x.off = x.Lk - x.L;
+        x.ntk = cdiv(x.Lk, kTile);
+        x.i0 = p.causal ? max(0, floor_div(x.j * kTile - x.off, kTile)) : 0;
+        x.ni = max(0, x.nt - x.i0);  // 0 only when the sequence has no queries
+    } else {
+        x.tk0 = x.t0;
+        x.Lk = x.L;
+        x.off = 0;
+        x.ntk = x.nt;
+        x.i0 = p.causal ? x.j : 0;
+        x.ni = p.causal ? x.nt - x.j : x.nt;
+    }
     return x;
 }
 
@@ -129,16 +141,19 @@ __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
 // In atomic mode every unit of a (sequence, head) walks the tiles in the same
 // order, so units running side by side load the same Q/dO tile and reduce into
 // the same dQ tile while it is resident in L2.
+template <bool KV>
 __device__ __forceinline__ int walk_tile(const BUnit& x, int s, int deterministic, int causal) {
     if (!causal) return s;
-    return deterministic ? x.i0 + s : x.nt - 1 - s;
+    return deterministic ? (KV ? x.i0 : x.j) + s : x.nt - 1 - s;
 }
 
 // Deterministic mode: how many contributions to dQ tile i precede unit x's.
 // Contributions arrive in descending key/value tile: from jmax(i), ..., 0,
 // where jmax(i) is the last key/value tile a row of query tile i sees (i for
 // equal lengths under the causal mask; ntk - 1 without it).
+template <bool KV>
 __device__ __forceinline__ int dq_rank(const BUnit& x, int i, int causal) {
+    if constexpr (!KV) return causal ? i - x.j : x.nt - 1 - x.j;
     const int jmax = causal ? min(x.ntk - 1, floor_div((i + 1) * kTile + x.off - 1, kTile))
                             : x.ntk - 1;
     return jmax - x.j;
@@ -228,7 +243,7 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* l
     }
 }
 
-template <int D>
+template <int D, bool KV>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
     pdl_trigger();
@@ -322,7 +337,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             unit.y = __shfl_sync(0xffffffffu, unit.y, 0);
             ++sched_it;
             if (unit.x < 0) break;
-            const BUnit x = decode_bunit(unit, p);
+            const BUnit x = decode_bunit<KV>(unit, p);
             if (!(ok = lane0_wait(smem_u32(&sm.kv_empty), (unit_it & 1) ^ 1, abort_flag, hdr)))
                 break;
             if (lane == 0) {
@@ -337,7 +352,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             ++unit_it;
             for (int s = 0; s < x.ni && ok; ++s, ++c) {
-                const int i = walk_tile(x, s, p.deterministic, p.causal);
+                const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
                 const int st = c & 1;
                 // Q_i (with its LSE and D rows) into the 2-stage ring
                 if (!(ok = lane0_wait(smem_u32(&sm.q_empty[st]), ((c >> 1) & 1) ^ 1, abort_flag,
@@ -393,9 +408,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(smem_u32(&sm.sched_empty[slot]));
                 ++sched_it;
                 if (unit.x < 0) break;
-                const BUnit x = decode_bunit(unit, p);
+                const BUnit x = decode_bunit<KV>(unit, p);
                 for (int s = 0; s < x.ni; ++s, ++c) {
-                    const int i = walk_tile(x, s, p.deterministic, p.causal);
+                    const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
                     if (!(ok = wait_or_abort(smem_u32(&sm.do_empty), (c & 1) ^ 1, abort_flag, hdr)))
                         break;
                     const uint32_t dbar = smem_u32(&sm.do_full);
@@ -446,9 +461,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(smem_u32(&sm.sched_empty[slot]));
                 ++sched_it;
                 if (unit.x < 0) break;
-                const BUnit x = decode_bunit(unit, p);
+                const BUnit x = decode_bunit<KV>(unit, p);
                 if (!(ok = wait_or_abort(smem_u32(&sm.kv_full), unit_it & 1, abort_flag, hdr))) break;
-                if (x.ni > 0 && !(ok = issue_s(cnt))) break;
+                if ((!KV || x.ni > 0) && !(ok = issue_s(cnt))) break;
                 for (int s = 0; s < x.ni; ++s, ++cnt) {
                     const int st = cnt & 1;
                     const uint32_t qaddr = smem_u32(sm.q[st]);
@@ -598,15 +613,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
             ++sched_it;
             if (unit.x < 0) break;
-            const BUnit x = decode_bunit(unit, p);
-            const int c = x.j * kTile + rk;  // key position within its sequence
+            const BUnit x = decode_bunit<KV>(unit, p);
+            // key position c within its sequence: query column r sees it iff
+            // r >= c - off (causal) and r < L; a key past the end sees nothing
+            const int c = x.j * kTile + rk;
+            const int c_off = c - x.off;
+            const int L_vis = c < x.Lk ? x.L : 0;  // (KV only)
             for (int s = 0; s < x.ni; ++s, ++cnt) {
-                const int i = walk_tile(x, s, p.deterministic, p.causal);
+                const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
                 const int st = cnt & 1;
                 // visible query columns of this key row: [lo, hi); the warp skips the
                 // mask when every row sees every column
-                const int lo = p.causal ? max(0, c - x.off - i * kTile) : 0;
-                const int hi = c < x.Lk ? min(kTile, x.L - i * kTile) : 0;
+                int lo, hi;
+                if constexpr (KV) {
+                    lo = p.causal ? max(0, c_off - i * kTile) : 0;
+                    hi = min(kTile, L_vis - i * kTile);
+                } else {
+                    lo = p.causal ? max(0, c - i * kTile) : 0;
+                    hi = c < x.L ? min(kTile, x.L - i * kTile) : 0;
+                }
                 const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kTile);
                 if (!(ok = warp_wait(smem_u32(&sm.q_full[st]), (cnt >> 1) & 1, abort_flag, hdr)))
                     break;
@@ -705,9 +730,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
             ++sched_it;
             if (unit.x < 0) break;
-            const BUnit x = decode_bunit(unit, p);
+            const BUnit x = decode_bunit<KV>(unit, p);
             for (int s = 0; s < x.ni; ++s) {
-                const int i = walk_tile(x, s, p.deterministic, p.causal);
+                const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
                 if (!(ok = wg_wait(smem_u32(&sm.dq_full), cnt & 1, abort_flag, hdr))) break;
                 tc_fence_after();
                 int* sem = nullptr;
@@ -715,7 +740,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (p.deterministic) {
                     sem = sems + (size_t)x.h * n_qtiles + tile_off[x.b] + i;
                     if (leader) {
-                        sem_ok = sem_wait(sem, dq_rank(x, i, p.causal), hdr);
+                        sem_ok = sem_wait(sem, dq_rank<KV>(x, i, p.causal), hdr);
                         if (!sem_ok) raise_abort(abort_flag, hdr, kErrTimeout);
                     }
                     sem_ok = named_bar_and(1, 128, sem_ok);
@@ -787,7 +812,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int kr = x.j * kTile + rr;
             const bool valid = kr < x.Lk;
             const size_t tok = (size_t)x.tk0 + (size_t)kr;
-            const bool none = x.ni == 0;  // no query: dK = dV = 0, TMEM was not written
+            const bool none = KV && x.ni == 0;  // no query: dK = dV = 0, TMEM not written
             const bool gqa = p.Hq != p.Hkv;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
@@ -977,7 +1002,7 @@ int grid_for(long long work, int threads, int num_sms) {
 
 template <int D>
 cudaError_t launch_bwd_t(const BwdParams& p, int num_sms, cudaStream_t stream) {
-    auto kern = fa_bwd_kernel<D>;
+    auto kern = p.kv ? fa_bwd_kernel<D, true> : fa_bwd_kernel<D, false>;
     const size_t smem = sizeof(BwdSmem<D>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -80,9 +80,12 @@ struct FwdSmem {
 // query row r sees key c iff c <= r + Lk - L.  n[t] = key/value tiles query
 // tile t visits (0 when the tile is past the end, or sees no key at all).
 struct UnitGeom {
-    int b, m, h, g, t0, L, tk0, Lk, n[2], nkv;
+    int b, m, h, g, t0, L, tk0, Lk, n[2], nkv;  // nkv >= 1 (see decode_unit)
 };
 
+// KV = false: keys and queries share their boundaries (Lk = L, tk0 = t0), and
+// the geometry is the plain square one.
+template <bool KV>
 __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
     UnitGeom x;
     x.b = u.x;
@@ -90,7 +93,12 @@ __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
     x.h = unit_head(u.y);
     x.g = (int)(((long long)x.h * p.Hkv) / p.Hq);
     seq_bounds(p.cu_seqlens, p.N, x.b, x.t0, x.L);
-    seq_bounds(p.cu_seqlens_k, p.Nk, x.b, x.tk0, x.Lk);
+    if constexpr (KV) {
+        seq_bounds(p.cu_seqlens_k, p.Nk, x.b, x.tk0, x.Lk);
+    } else {
+        x.tk0 = x.t0;
+        x.Lk = x.L;
+    }
     const int r0 = x.m * kFwdBlockRows;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -99,12 +107,16 @@ __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
             x.n[t] = 0;
         } else if (p.causal) {
             const int re = min(rs + kTile, x.L);  // one past last valid row
-            x.n[t] = cdiv(max(re + x.Lk - x.L, 0), kTile);
+            x.n[t] = KV ? cdiv(max(re + x.Lk - x.L, 0), kTile) : cdiv(re, kTile);
         } else {
             x.n[t] = cdiv(x.Lk, kTile);
         }
     }
-    x.nkv = max(x.n[0], x.n[1]);
+    // A unit whose rows see no key (KV only) still takes one key/value step
+    // with both query tiles masked off (no MMA issued): the producer and MMA
+    // thread then keep their usual barrier sequence, and the softmax warps
+    // write O = 0.
+    x.nkv = KV ? max(max(x.n[0], x.n[1]), 1) : max(x.n[0], x.n[1]);
     return x;
 }
 
@@ -159,7 +171,7 @@ __device__ __forceinline__ void write_keyless_row(const FwdParams& p, int h, siz
     }
 }
 
-template <int D, bool OUT_FP32>
+template <int D, bool OUT_FP32, bool KV>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     pdl_trigger();
@@ -231,14 +243,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 mbar_arrive(smem_u32(&sm.sched_full[slot]));
                 ++sched_it;
                 if (unit.x < 0) break;
-                const UnitGeom x = decode_unit(unit, p);
+                const UnitGeom x = decode_unit<KV>(unit, p);
                 const int row0 = x.t0 + x.m * kFwdBlockRows;
                 if (!(ok = wait_or_abort(smem_u32(&sm.q_empty), (unit_it & 1) ^ 1, abort_flag, hdr)))
                     break;
                 // only the query tiles that see a key are loaded (none when no row of
-                // the unit sees one: the barrier then completes on the arrival alone)
+                // the unit sees one: the barrier then completes on the arrival alone;
+                // such a unit still loads one key/value tile, which nothing reads)
                 const uint32_t qbar = smem_u32(&sm.q_full);
-                mbar_arrive_expect_tx(qbar, ((x.n[0] > 0) + (x.n[1] > 0)) * Cfg::kTileBytes);
+                if constexpr (KV)
+                    mbar_arrive_expect_tx(qbar, ((x.n[0] > 0) + (x.n[1] > 0)) * Cfg::kTileBytes);
+                else
+                    mbar_arrive_expect_tx(qbar, (x.n[1] > 0 ? 2 : 1) * Cfg::kTileBytes);
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (x.n[t] == 0) continue;
@@ -293,7 +309,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 mbar_arrive(smem_u32(&sm.sched_empty[slot]));
                 ++sched_it;
                 if (unit.x < 0) break;
-                const UnitGeom x = decode_unit(unit, p);
+                const UnitGeom x = decode_unit<KV>(unit, p);
                 if (!(ok = wait_or_abort(smem_u32(&sm.q_full), unit_it & 1, abort_flag, hdr)))
                     break;
                 for (int j = 0; j < x.nkv && ok; ++j) {
@@ -348,7 +364,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     ++kv_it;
                 }
                 if (!ok) break;
-                if (x.nkv == 0) mma_commit(smem_u32(&sm.q_empty));  // no key: Q was not loaded
                 ++unit_it;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) ep[t] += x.n[t] > 0;
@@ -378,17 +393,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
             ++sched_it;
             if (unit.x < 0) break;
-            const UnitGeom x = decode_unit(unit, p);
+            const UnitGeom x = decode_unit<KV>(unit, p);
             const int nt = t == 0 ? x.n[0] : x.n[1];
+            if constexpr (!KV) {
+                if (nt == 0) continue;  // the tile is past the end
+            }
             const int r = x.m * kFwdBlockRows + t * kTile + row;  // row within the sequence
-            if (nt == 0) {
-                // the tile is past the end, or none of its rows sees a key (more
-                // queries than keys): O = 0 and LSE = -inf, nothing on chip
-                if (r < x.L) write_keyless_row<D, OUT_FP32>(p, x.h, (size_t)x.t0 + (size_t)r);
-                continue;
+            if constexpr (KV) {
+                if (nt == 0) {
+                    // the tile is past the end, or none of its rows sees a key:
+                    // O = 0 and LSE = -inf, nothing on chip
+                    if (r < x.L) write_keyless_row<D, OUT_FP32>(p, x.h, (size_t)x.t0 + (size_t)r);
+                    continue;
+                }
             }
             // visible keys: col < limit (end-aligned causal mask)
-            const int limit = p.causal ? min(r + 1 + x.Lk - x.L, x.Lk) : x.Lk;
+            const int limit = KV ? (p.causal ? min(r + 1 + x.Lk - x.L, x.Lk) : x.Lk)
+                                 : (p.causal ? min(r + 1, x.L) : x.L);
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < nt; ++j) {
                 if (!(ok = warp_wait(smem_u32(&sm.s_full[t]), it & 1, abort_flag, hdr))) break;
@@ -480,7 +501,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!(ok = warp_wait(smem_u32(&sm.o_done[t]), (it - 1) & 1, abort_flag, hdr))) break;
             tc_fence_after();
             const bool valid = r < x.L;
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;  // l = 0: the row sees no key
+            // l = 0 only for a KV row that sees no key
+            const float inv_l = KV ? (l > 0.f ? 1.f / l : 0.f) : 1.f / l;
             const size_t tok = (size_t)x.t0 + (size_t)r;
             if (valid) p.lse[(size_t)x.h * p.T + tok] = (m_ref + __log2f(l)) * 0.69314718055994531f;
 #pragma unroll 1
@@ -530,9 +552,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
 }
 
-template <int D, bool F32>
+template <int D, bool F32, bool KV>
 cudaError_t launch_fwd_t(const FwdParams& p, int num_sms, cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D, F32>;
+    auto kern = fa_fwd_kernel<D, F32, KV>;
     const size_t smem = sizeof(FwdSmem<D>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -544,12 +566,18 @@ cudaError_t launch_fwd_t(const FwdParams& p, int num_sms, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_fwd(const FwdParams& p, int num_sms, cudaStream_t stream) {
+template <bool KV>
+cudaError_t launch_fwd_kv(const FwdParams& p, int num_sms, cudaStream_t stream) {
     if (p.d == 128)
-        return p.o_fp32 ? launch_fwd_t<128, true>(p, num_sms, stream)
-                        : launch_fwd_t<128, false>(p, num_sms, stream);
-    return p.o_fp32 ? launch_fwd_t<64, true>(p, num_sms, stream)
-                    : launch_fwd_t<64, false>(p, num_sms, stream);
+        return p.o_fp32 ? launch_fwd_t<128, true, KV>(p, num_sms, stream)
+                        : launch_fwd_t<128, false, KV>(p, num_sms, stream);
+    return p.o_fp32 ? launch_fwd_t<64, true, KV>(p, num_sms, stream)
+                    : launch_fwd_t<64, false, KV>(p, num_sms, stream);
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int num_sms, cudaStream_t stream) {
+    return p.kv ? launch_fwd_kv<true>(p, num_sms, stream)
+                : launch_fwd_kv<false>(p, num_sms, stream);
 }
 
 }  // namespace fa

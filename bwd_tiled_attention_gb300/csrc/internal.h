@@ -14,14 +14,15 @@ struct FwdParams {
     void* o;
     float* lse;
     const int* cu_seqlens;         // query sequences; null for dense
-    const int* cu_seqlens_k;       // key/value sequences; null for dense
     void* workspace;               // header + unit list
     size_t units_off;
     int B, Hq, Hkv, N, T, d;       // N, T: query length bound and tokens
-    int Nk, Tk;                    // key/value length bound and tokens
     float scale_log2;              // scale * log2(e)
     int causal;
     int o_fp32;
+    const int* cu_seqlens_k;       // key/value sequences; null for dense
+    int Nk, Tk;                    // key/value length bound and tokens
+    int kv;                        // key boundaries differ from the query ones
 };
 
 struct BwdParams {
@@ -32,16 +33,17 @@ struct BwdParams {
     void* dk;                      // final dK (MHA) -- bf16 or fp32
     void* dv;
     const int* cu_seqlens;         // query sequences; null for dense
-    const int* cu_seqlens_k;       // key/value sequences; null for dense
     void* workspace;
     size_t units_off, tile_off_off, sems_off, dq_acc_off, dk_acc_off, dv_acc_off;
     int B, Hq, Hkv, N, T, d;       // N, T: query length bound and tokens
-    int Nk, Tk;                    // key/value length bound and tokens
     float scale;                   // softmax scale (dK and dQ factor)
     float scale_log2;              // scale * log2(e)
     int causal;
     int deterministic;
     int grad_fp32;
+    const int* cu_seqlens_k;       // key/value sequences; null for dense
+    int Nk, Tk;                    // key/value length bound and tokens
+    int kv;                        // key boundaries differ from the query ones
 };
 
 // Writes the unit list over the tiles of `cu_seqlens` / N (T tokens) and,

@@ -38,6 +38,7 @@ class Workload:
     qk_scale: float = 1.0           # Q and K multiplied by this before rounding
     o_fp32: bool = False            # forward writes an fp32 O
     deterministic: bool = False     # backward in deterministic mode
+    lengths_k: list | None = None   # key/value lengths, when they differ from the query lengths
     extra: dict = field(default_factory=dict)
 
     @property
@@ -62,6 +63,7 @@ def workloads() -> dict:
                                N=8192),
         "varlen_det": Workload("varlen_det", B=16, Hq=16, Hkv=16, d=128, causal=True, seed=4,
                                len_range=(256, 8192), deterministic=True),
+        **kv_workloads(),
     }
 
 
@@ -104,6 +106,11 @@ def make_inputs(B, Hq, Hkv, d, seed, N=None, lengths=None, len_range=None, qk_sc
 
 def make_workload(w: Workload, **override):
     """Inputs for a named workload (fields may be overridden, e.g. N=256)."""
+    if w.lengths_k is not None:
+        kw = dict(Hq=w.Hq, Hkv=w.Hkv, d=w.d, seed=w.seed, lengths_q=w.lengths,
+                  lengths_k=w.lengths_k, qk_scale=w.qk_scale)
+        kw.update(override)
+        return make_inputs_kv(**kw)
     kw = dict(B=w.B, Hq=w.Hq, Hkv=w.Hkv, d=w.d, seed=w.seed, qk_scale=w.qk_scale)
     if w.len_range is not None:
         kw["len_range"] = w.len_range
@@ -141,17 +148,16 @@ def make_inputs_kv(Hq, Hkv, d, seed, lengths_q, lengths_k, qk_scale=1.0):
 
 
 def kv_workloads() -> dict:
-    """Named workloads with different query and key lengths: (B, Hq, Hkv, d,
-    causal, seed, lengths_q, lengths_k).  ``chunk_causal``: 2048 new tokens per
-    sequence against 8192 keys (6144 earlier positions plus the new ones);
-    ``varlen_chunks``: packed sequences whose key length is the query length
-    plus a drawn number of earlier positions."""
+    """Named workloads with different query and key lengths.  ``chunk_causal``:
+    2048 new tokens per sequence against 8192 keys (6144 earlier positions plus
+    the new ones); ``varlen_chunks``: packed sequences whose key length is the
+    query length plus a drawn number of earlier positions."""
     gen = torch.Generator().manual_seed(9)
     lq = [int(x) for x in torch.randint(1, 2049, (8,), generator=gen)]
     extra = [int(x) for x in torch.randint(0, 6145, (8,), generator=gen)]
     return {
-        "chunk_causal": dict(B=4, Hq=16, Hkv=16, d=128, causal=True, seed=5,
-                             lengths_q=[2048] * 4, lengths_k=[8192] * 4),
-        "varlen_chunks": dict(B=8, Hq=16, Hkv=4, d=128, causal=True, seed=6, lengths_q=lq,
-                              lengths_k=[a + b for a, b in zip(lq, extra)]),
+        "chunk_causal": Workload("chunk_causal", B=4, Hq=16, Hkv=16, d=128, causal=True, seed=5,
+                                 lengths=[2048] * 4, lengths_k=[8192] * 4),
+        "varlen_chunks": Workload("varlen_chunks", B=8, Hq=16, Hkv=4, d=128, causal=True, seed=6,
+                                  lengths=lq, lengths_k=[a + b for a, b in zip(lq, extra)]),
     }

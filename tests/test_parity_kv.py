@@ -119,22 +119,21 @@ def test_kv_entry_with_equal_lengths_matches_equal_length_entry():
 def _sampled_check(w, inp, got, rng):
     oi = oracle_inputs(inp)
     cu_q, cu_k = inp["cu_seqlens"].numpy(), inp["cu_seqlens_k"].numpy()
-    scale = 1.0 / np.sqrt(w["d"])
-    B = len(w["lengths_q"])
+    B = len(w.lengths)
     for b in sorted({0, B - 1, int(rng.integers(0, B))}):
         Lq, Lk = int(cu_q[b + 1] - cu_q[b]), int(cu_k[b + 1] - cu_k[b])
-        h = int(rng.integers(0, w["Hq"]))
+        h = int(rng.integers(0, w.Hq))
         rows = np.unique(np.concatenate([[0, Lq - 1], rng.integers(0, Lq, 16)]))
-        ref = oracle.rows(oi["q"], oi["k"], oi["v"], cu_q, scale, w["causal"], b, h, rows,
+        ref = oracle.rows(oi["q"], oi["k"], oi["v"], cu_q, w.scale, w.causal, b, h, rows,
                           dout=oi["dout"], cu_seqlens_k=cu_k)
         t = cu_q[b] + rows
         assert_close(f"o b{b} h{h}", to_np(got["o"][t, h]), ref["o"])
         assert_lse_kv(to_np(got["lse"][h, t]), ref["lse"])
         assert_close(f"dq b{b} h{h}", to_np(got["dq"][t, h]), ref["dq"])
-        g = int(rng.integers(0, w["Hkv"]))
+        g = int(rng.integers(0, w.Hkv))
         lo = int(Lk * 0.8)
         keys = np.unique(np.concatenate([[lo, Lk - 1], rng.integers(lo, Lk, 8)]))
-        kg = oracle.key_grads(oi["q"], oi["k"], oi["v"], oi["dout"], cu_q, scale, w["causal"], b,
+        kg = oracle.key_grads(oi["q"], oi["k"], oi["v"], oi["dout"], cu_q, w.scale, w.causal, b,
                               g, keys, cu_seqlens_k=cu_k)
         t = cu_k[b] + keys
         assert_close(f"dk b{b} g{g}", to_np(got["dk"][t, g]), kg["dk"])
@@ -144,14 +143,13 @@ def _sampled_check(w, inp, got, rng):
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["chunk_causal", "varlen_chunks"])
 def test_kv_workloads_sampled(name):
-    w = synth.kv_workloads()[name]
-    inp, x = kv_inputs(w["lengths_q"], w["lengths_k"], w["Hq"], w["Hkv"], w["d"], w["seed"])
-    scale = 1.0 / np.sqrt(w["d"])
-    got = run_kv(x, w["lengths_q"], w["lengths_k"], w["causal"], scale)
+    w = synth.workloads()[name]
+    inp, x = kv_inputs(w.lengths, w.lengths_k, w.Hq, w.Hkv, w.d, w.seed)
+    got = run_kv(x, w.lengths, w.lengths_k, w.causal, w.scale)
     _sampled_check(w, inp, got, np.random.default_rng(8))
-    det = run_kv(x, w["lengths_q"], w["lengths_k"], w["causal"], scale, deterministic=True)
+    det = run_kv(x, w.lengths, w.lengths_k, w.causal, w.scale, deterministic=True)
     _sampled_check(w, inp, det, np.random.default_rng(9))
     for _ in range(3):
-        again = run_kv(x, w["lengths_q"], w["lengths_k"], w["causal"], scale, deterministic=True)
+        again = run_kv(x, w.lengths, w.lengths_k, w.causal, w.scale, deterministic=True)
         for k in ("dq", "dk", "dv"):
             assert torch.equal(det[k].view(torch.int16), again[k].view(torch.int16))
