@@ -161,3 +161,28 @@ def kv_workloads() -> dict:
         "varlen_chunks": Workload("varlen_chunks", B=8, Hq=16, Hkv=4, d=128, causal=True, seed=6,
                                   lengths=lq, lengths_k=[a + b for a, b in zip(lq, extra)]),
     }
+
+
+def make_inputs_device(Hq, Hkv, d, seed, lengths, device, lengths_k=None):
+    """Like ``make_inputs`` / ``make_inputs_kv`` but drawn on ``device`` with
+    torch's seeded generator for that device, for sizes whose host copies would
+    not fit comfortably (tens of GB).  Same draw order (Q, K, V, dO in float32,
+    then bf16 rounding).  Checks copy the slices they compare to the host."""
+    gen = torch.Generator(device=device).manual_seed(int(seed))
+    lengths = [int(x) for x in lengths]
+    lengths_k = lengths if lengths_k is None else [int(x) for x in lengths_k]
+    Tq, Tk = sum(lengths), sum(lengths_k)
+    out = {}
+    for name, T, H in (("q", Tq, Hq), ("k", Tk, Hkv), ("v", Tk, Hkv), ("dout", Tq, Hq)):
+        t = torch.empty((T, H, d), dtype=torch.bfloat16, device=device)
+        # draw in chunks of rows so the float32 temporary stays small
+        step = max(1, (1 << 26) // (H * d))
+        for r0 in range(0, T, step):
+            r1 = min(T, r0 + step)
+            t[r0:r1] = torch.randn((r1 - r0, H, d), generator=gen, device=device,
+                                   dtype=torch.float32).to(torch.bfloat16)
+        out[name] = t
+    out["cu_seqlens"] = cu_from_lengths(lengths).to(device)
+    out["cu_seqlens_k"] = cu_from_lengths(lengths_k).to(device)
+    out["lengths"], out["lengths_k"] = lengths, lengths_k
+    return out
