@@ -108,7 +108,7 @@ fa_status check_shape(int B, int Hq, int Hkv, int Nq, int total_q, int Nk, int t
     if (B < 0 || Hq <= 0 || Hkv <= 0) return FA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if (Hq > kMaxHeads) return FA_ERR_UNSUPPORTED;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
     if ((cu_q == nullptr) != (cu_k == nullptr)) return FA_ERR_INVALID_ARG;
     s.B = B; s.Hq = Hq; s.Hkv = Hkv; s.Nq = Nq; s.Nk = Nk; s.d = d;
     s.varlen = cu_q != nullptr;
@@ -184,7 +184,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, fa_dtyp
 size_t bwd_ws_bytes(int B, int Hq, int Hkv, int Nq, int total_q, int Nk, int total_k, int d,
                     bool sems_offset) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || total_q < 0 || Nk < 0 || total_k < 0 ||
-        (d != 64 && d != 128))
+        (d != 64 && d != 96 && d != 128))
         return 0;
     const long long Tq = total_q > 0 ? total_q : (long long)B * Nq;
     const long long Tk = total_k > 0 ? total_k : (long long)B * Nk;

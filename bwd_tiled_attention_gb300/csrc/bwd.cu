@@ -243,7 +243,11 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* l
     }
 }
 
-template <int D, bool KV>
+// D: the tile layout (64 or 128 columns); DR: the head dimension in memory.
+// DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros,
+// which add nothing to S or dP and make the last 32 columns of dV, dK and dQ
+// zero; those columns are neither stored nor merged.
+template <int D, int DR, bool KV>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
     pdl_trigger();
@@ -750,9 +754,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // back at once: the next step's dP MMA waits for them.
                 const bool whole = row0 + kTile <= x.L;
                 const int qr = row0 + rr;
-                uint32_t v[D / 32][32];
+                uint32_t v[DR / 32][32];
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc)
+                for (int cc = 0; cc < DR / 32; ++cc)
                     tmem_ld32(tmem + lane_off + Cfg::kColDQ + cc * 32, v[cc]);
                 tmem_ld_wait();
                 tc_fence_before();
@@ -762,7 +766,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // Whole tile: bulk reduce-add, one 32-column chunk at a time,
                     // staged 128B-swizzled through two 16 KB slots.
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc, ++chunk) {
+                    for (int cc = 0; cc < DR / 32; ++cc, ++chunk) {
                         const int sl = chunk & 1;
                         // the reduce that last used this slot has read it
                         if (leader) bulk_wait_group_read<1>();
@@ -782,9 +786,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                 } else if (qr < x.L && sem_ok) {
                     // Ragged last tile of a sequence: per-row vector reductions.
-                    float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * D;
+                    float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * DR;
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc)
+                    for (int cc = 0; cc < DR / 32; ++cc)
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[cc][4 * e]),
@@ -819,7 +823,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t col = which == 0 ? Cfg::kColDK : Cfg::kColDV;
                 const float mul = which == 0 ? p.scale : 1.f;
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < DR / 32; ++cc) {
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_off + col + cc * 32, v);
                     tmem_ld_wait();
@@ -829,7 +833,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         for (int e = 0; e < 32; ++e) v[e] = 0u;
                     }
                     if (gqa) {
-                        float* acc = (which == 0 ? dk_acc : dv_acc) + (tok * p.Hq + x.h) * D + cc * 32;
+                        float* acc = (which == 0 ? dk_acc : dv_acc) + (tok * p.Hq + x.h) * DR + cc * 32;
                         float4* d4 = reinterpret_cast<float4*>(acc);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
@@ -839,7 +843,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                 __uint_as_float(v[4 * e + 3]) * mul);
                     } else if (p.grad_fp32) {
                         float* out = static_cast<float*>(which == 0 ? p.dk : p.dv) +
-                                     (tok * p.Hkv + x.g) * D + cc * 32;
+                                     (tok * p.Hkv + x.g) * DR + cc * 32;
                         float4* d4 = reinterpret_cast<float4*>(out);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
@@ -849,7 +853,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                 __uint_as_float(v[4 * e + 3]) * mul);
                     } else {
                         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(which == 0 ? p.dk : p.dv) +
-                                             (tok * p.Hkv + x.g) * D + cc * 32;
+                                             (tok * p.Hkv + x.g) * DR + cc * 32;
                         uint4* d4 = reinterpret_cast<uint4*>(out);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -887,13 +891,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // D = rowsum(dO * O) per (token, head); zero the dQ accumulator row and the
 // semaphores.  Each lane takes 8 elements (16-byte loads), D/8 lanes per row,
 // so a warp covers 32/(D/8) rows per pass.
-template <int D, bool O_FP32>
+template <int D, bool O_FP32>  // D: the head dimension in memory (64, 96 or 128)
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const void* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                           float* __restrict__ Dout, float* __restrict__ dq_acc,
                           int* __restrict__ sems, long long n_sems, int T, int Hq) {
     pdl_begin();
-    constexpr int LPR = D / 8;     // lanes per row
+    constexpr int LPR = D == 96 ? 16 : D / 8;  // lanes per row (a power of two)
     constexpr int RPW = 32 / LPR;  // rows per warp pass
     const long long rows = (long long)T * Hq;
     const long long warp_g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -904,7 +908,7 @@ __global__ void __launch_bounds__(256)
         const long long r = r0 + sub;
         const bool valid = r < rows;
         float acc = 0.f;
-        if (valid) {
+        if (valid && l * 8 < D) {  // (lanes past the row idle when D = 96)
             const size_t base = (size_t)r * D + (size_t)l * 8;
             const uint4 dv = *reinterpret_cast<const uint4*>(dout + base);
             const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
@@ -1000,9 +1004,9 @@ int grid_for(long long work, int threads, int num_sms) {
     return (int)(g < 1 ? 1 : g);
 }
 
-template <int D>
+template <int D, int DR>
 cudaError_t launch_bwd_t(const BwdParams& p, int num_sms, cudaStream_t stream) {
-    auto kern = p.kv ? fa_bwd_kernel<D, true> : fa_bwd_kernel<D, false>;
+    auto kern = p.kv ? fa_bwd_kernel<D, DR, true> : fa_bwd_kernel<D, DR, false>;
     const size_t smem = sizeof(BwdSmem<D>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1027,6 +1031,8 @@ cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, f
                    dq_acc, sems, n_sems, T, Hq)
     if (d == 128) {
         if (o_fp32) FA_PRE(128, true); else FA_PRE(128, false);
+    } else if (d == 96) {
+        if (o_fp32) FA_PRE(96, true); else FA_PRE(96, false);
     } else {
         if (o_fp32) FA_PRE(64, true); else FA_PRE(64, false);
     }
@@ -1035,7 +1041,9 @@ cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, f
 }
 
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream) {
-    return p.d == 128 ? launch_bwd_t<128>(p, num_sms, stream) : launch_bwd_t<64>(p, num_sms, stream);
+    if (p.d == 128) return launch_bwd_t<128, 128>(p, num_sms, stream);
+    if (p.d == 96) return launch_bwd_t<128, 96>(p, num_sms, stream);
+    return launch_bwd_t<64, 64>(p, num_sms, stream);
 }
 
 cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const float* dk_acc,
@@ -1050,6 +1058,8 @@ cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const float* d
                    dk_acc, dv_acc, dk, dv, Tq, Tk, Hq, Hkv, scale)
     if (d == 128) {
         if (grad_fp32) FA_POST(128, true); else FA_POST(128, false);
+    } else if (d == 96) {
+        if (grad_fp32) FA_POST(96, true); else FA_POST(96, false);
     } else {
         if (grad_fp32) FA_POST(64, true); else FA_POST(64, false);
     }

@@ -158,20 +158,23 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // A query row that sees no key: O = 0, LSE = -inf.
-template <int D, bool OUT_FP32>
+template <int DR, bool OUT_FP32>
 __device__ __forceinline__ void write_keyless_row(const FwdParams& p, int h, size_t tok) {
     p.lse[(size_t)h * p.T + tok] = -INFINITY;
-    const size_t base = (tok * p.Hq + h) * D;
+    const size_t base = (tok * p.Hq + h) * DR;
     if (OUT_FP32) {
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base);
-        for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < DR / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     } else {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + base);
-        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < DR / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-template <int D, bool OUT_FP32, bool KV>
+// D: the tile layout (64 or 128 columns); DR: the head dimension in memory.
+// DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros,
+// which add nothing to S, and O's last 32 columns (all zero) are not stored.
+template <int D, int DR, bool OUT_FP32, bool KV>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     pdl_trigger();
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (nt == 0) {
                     // the tile is past the end, or none of its rows sees a key:
                     // O = 0 and LSE = -inf, nothing on chip
-                    if (r < x.L) write_keyless_row<D, OUT_FP32>(p, x.h, (size_t)x.t0 + (size_t)r);
+                    if (r < x.L) write_keyless_row<DR, OUT_FP32>(p, x.h, (size_t)x.t0 + (size_t)r);
                     continue;
                 }
             }
@@ -476,7 +479,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (__any_sync(0xffffffffu, need)) {
                     // O~ is stable here: S_t(j) was committed after O_t += P_t V of j-1.
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < DR / 32; ++c) {
                         uint32_t ov[32];
                         tmem_ld32(o_addr + c * 32, ov);
                         tmem_ld_wait();
@@ -506,12 +509,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const size_t tok = (size_t)x.t0 + (size_t)r;
             if (valid) p.lse[(size_t)x.h * p.T + tok] = (m_ref + __log2f(l)) * 0.69314718055994531f;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < DR / 32; ++c) {
                 uint32_t ov[32];
                 tmem_ld32(o_addr + c * 32, ov);
                 tmem_ld_wait();
                 if (valid) {
-                    const size_t base = (tok * p.Hq + x.h) * D + c * 32;
+                    const size_t base = (tok * p.Hq + x.h) * DR + c * 32;
                     if (OUT_FP32) {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base);
 #pragma unroll
@@ -552,9 +555,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
 }
 
-template <int D, bool F32, bool KV>
+template <int D, int DR, bool F32, bool KV>
 cudaError_t launch_fwd_t(const FwdParams& p, int num_sms, cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D, F32, KV>;
+    auto kern = fa_fwd_kernel<D, DR, F32, KV>;
     const size_t smem = sizeof(FwdSmem<D>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -569,10 +572,13 @@ cudaError_t launch_fwd_t(const FwdParams& p, int num_sms, cudaStream_t stream) {
 template <bool KV>
 cudaError_t launch_fwd_kv(const FwdParams& p, int num_sms, cudaStream_t stream) {
     if (p.d == 128)
-        return p.o_fp32 ? launch_fwd_t<128, true, KV>(p, num_sms, stream)
-                        : launch_fwd_t<128, false, KV>(p, num_sms, stream);
-    return p.o_fp32 ? launch_fwd_t<64, true, KV>(p, num_sms, stream)
-                    : launch_fwd_t<64, false, KV>(p, num_sms, stream);
+        return p.o_fp32 ? launch_fwd_t<128, 128, true, KV>(p, num_sms, stream)
+                        : launch_fwd_t<128, 128, false, KV>(p, num_sms, stream);
+    if (p.d == 96)
+        return p.o_fp32 ? launch_fwd_t<128, 96, true, KV>(p, num_sms, stream)
+                        : launch_fwd_t<128, 96, false, KV>(p, num_sms, stream);
+    return p.o_fp32 ? launch_fwd_t<64, 64, true, KV>(p, num_sms, stream)
+                    : launch_fwd_t<64, 64, false, KV>(p, num_sms, stream);
 }
 
 cudaError_t launch_fwd(const FwdParams& p, int num_sms, cudaStream_t stream) {

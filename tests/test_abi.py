@@ -53,7 +53,8 @@ def test_workspace_sizes(L):
     assert wg >= w + 2 * T * Hq * d * 4
     off = fa.fa_bwd_workspace_semaphore_offset(4, Hq, Hq, 2048, 0, d)
     assert 0 < off < w and off % 256 == 0
-    assert fa.fa_bwd_workspace_size(1, 4, 4, 16, 0, 96) == 0   # unsupported head dim
+    assert fa.fa_bwd_workspace_size(1, 4, 4, 16, 0, 256) == 0  # unsupported head dim
+    assert fa.fa_bwd_workspace_size(1, 4, 4, 16, 0, 96) > 0    # 96 runs on 128-column tiles
 
 
 FAKE = 0x10000          # 16-byte aligned non-null fake device address (never dereferenced)
@@ -69,7 +70,8 @@ def fwd_call(**kw):
 
 def test_fwd_rejects_bad_arguments(L):
     assert fwd_call(Hkv=3) == fa.FA_ERR_INVALID_ARG            # Hq % Hkv != 0
-    assert fwd_call(d=96) == fa.FA_ERR_UNSUPPORTED              # head dim
+    assert fwd_call(d=256) == fa.FA_ERR_UNSUPPORTED             # head dim
+    assert fwd_call(d=80) == fa.FA_ERR_UNSUPPORTED
     assert fwd_call(q=FAKE + 8) == fa.FA_ERR_INVALID_ARG        # TMA needs 16-byte alignment
     assert fwd_call(lse=None) == fa.FA_ERR_INVALID_ARG          # null output
     assert fwd_call(workspace_bytes=8) == fa.FA_ERR_INVALID_ARG

@@ -78,7 +78,7 @@ def check_whole_head(w, inp, got, b, h):
     assert_lse(to_np(got["lse"][h, s0:s1]), ref["lse"][0])
 
 
-@pytest.mark.parametrize("name", ["mid_dense", "mid_causal"])
+@pytest.mark.parametrize("name", ["mid_dense", "mid_causal", "mid_causal_d96"])
 def test_mid(name):
     w = synth.workloads()[name]
     inp = synth.make_workload(w)

@@ -26,6 +26,7 @@ CASES = [
     ("more_queries", [300, 200, 129], [129, 64, 1], 4, 4, 128),
     ("d64_mqa", [256, 100, 5], [700, 100, 383], 6, 1, 64),
     ("empty_sides", [0, 50, 128, 0], [200, 0, 128, 0], 2, 2, 128),
+    ("d96", [129, 300], [700, 300], 4, 2, 96),
 ]
 
 

@@ -19,6 +19,7 @@ CASES = [
     ("varlen_edges", [1, 127, 128, 129, 255, 256, 257, 600], 4, 2, 128),
     ("varlen_d64_mqa", [5, 200, 384, 70], 6, 1, 64),
     ("gqa4_512", [512, 512], 8, 2, 128),
+    ("d96_gqa3", [1, 200, 384, 129], 6, 2, 96),
 ]
 
 
