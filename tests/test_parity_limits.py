@@ -3,6 +3,8 @@
 - Offsets past 2^31 elements: a packed batch of 2049 sequences x 8 heads x
   d = 128 (T*H*d > 2^31 in every token-major tensor) -- the first and the last
   sequences are checked whole.
+- 4096 packed sequences (the scheduler's limit) of lengths 1..300, GQA,
+  sampled sequences whole, atomic and deterministic.
 - One 131072-token causal sequence (1024 tiles per sequence, MQA): rows near
   both ends and keys near the end, atomic and deterministic, and the
   deterministic backward bit-identical over a repeat.
@@ -80,3 +82,30 @@ def test_longest_sequence_mqa():
     for det in (False, True):
         assert_close(f"dk det={det}", f64(grads[det][1][keys, 0]), kg["dk"])
         assert_close(f"dv det={det}", f64(grads[det][2][keys, 0]), kg["dv"])
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_largest_packed_batch(deterministic):
+    """4096 sequences (the scheduler's limit), lengths 1..300, GQA: the
+    one-CTA ranking of the scheduler at full size and thousands of ragged
+    tiles; sampled sequences against the oracle."""
+    gen = np.random.default_rng(34)
+    lengths = [int(x) for x in gen.integers(1, 301, 4096)]
+    Hq, Hkv, d = 4, 2, 64
+    x = synth.make_inputs_device(Hq, Hkv, d, 35, lengths, "cuda")
+    scale = 1.0 / np.sqrt(d)
+    kw = dict(cu_seqlens=x["cu_seqlens"], max_seqlen=max(lengths))
+    o, lse = fa.forward(x["q"], x["k"], x["v"], causal=True, scale=scale, **kw)
+    dq, dk, dv = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=True,
+                             scale=scale, deterministic=deterministic, check_status=True, **kw)
+    torch.cuda.synchronize()
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    for b in sorted({0, 1, 4095, int(np.argmax(lengths)), int(np.argmin(lengths)),
+                     *gen.integers(0, 4096, 5).tolist()}):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        sl = lambda t: f64(t[s0:s1])
+        ref = oracle.attention(sl(x["q"]), sl(x["k"]), sl(x["v"]), [0, s1 - s0], scale, True,
+                               dout=sl(x["dout"]))
+        for name, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+            assert_close(f"{name} b{b}", f64(t[s0:s1]), ref[name])
+        assert_lse(f64(lse[:, s0:s1]), ref["lse"])
