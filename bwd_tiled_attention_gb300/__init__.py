@@ -243,6 +243,52 @@ def _geometry(q, k, cu_seqlens, max_seqlen, batch):
     return B, Hq, Hkv, N, T, d
 
 
+def _check_tensor(name, t, dtypes, ndim):
+    """The tensor API passes raw device pointers: every tensor must be a
+    contiguous tensor of the expected dtype and rank (and, checked last by
+    _check_inputs, on a CUDA device)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must be {' or '.join(str(x) for x in dtypes)}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_inputs(q, k, v, cu_seqlens, cu_seqlens_k, dout=None, o=None, lse=None):
+    bf16 = (torch.bfloat16,)
+    _check_tensor("q", q, bf16, 3)
+    _check_tensor("k", k, bf16, 3)
+    _check_tensor("v", v, bf16, 3)
+    if k.shape != v.shape:
+        raise ValueError(f"k {tuple(k.shape)} and v {tuple(v.shape)} differ in shape")
+    if k.shape[2] != q.shape[2]:
+        raise ValueError("q and k differ in head dimension")
+    if q.shape[1] % k.shape[1] != 0:
+        raise ValueError("the query heads must be a multiple of the key/value heads")
+    for name, t in (("cu_seqlens", cu_seqlens), ("cu_seqlens_k", cu_seqlens_k)):
+        if t is not None:
+            _check_tensor(name, t, (torch.int32,), 1)
+    if dout is not None:
+        _check_tensor("dout", dout, bf16, 3)
+        if dout.shape != q.shape:
+            raise ValueError("dout must have the shape of q")
+    if o is not None:
+        _check_tensor("o", o, (torch.bfloat16, torch.float32), 3)
+        if o.shape != q.shape:
+            raise ValueError("o must have the shape of q")
+    if lse is not None:
+        _check_tensor("lse", lse, (torch.float32,), 2)
+        if tuple(lse.shape) != (q.shape[1], q.shape[0]):
+            raise ValueError("lse must be [Hq, Tq]")
+    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens", cu_seqlens),
+                    ("cu_seqlens_k", cu_seqlens_k), ("dout", dout), ("o", o), ("lse", lse)):
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be on a CUDA device")
+
+
 def _geometry_kv(q, k, cu_seqlens, max_seqlen, cu_seqlens_k, max_seqlen_k, batch):
     """(B, Hq, Hkv, Nq, Tq, Nk, Tk, d, kv): kv is True when queries and keys
     have separate lengths (the *_kv entry points)."""
@@ -270,6 +316,7 @@ def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, max_seqlen=None,
             out_dtype=torch.bfloat16, stream=None, workspace=None, cu_seqlens_k=None,
             max_seqlen_k=None):
     """Attention forward through the C ABI; returns (o, lse)."""
+    _check_inputs(q, k, v, cu_seqlens, cu_seqlens_k)
     B, Hq, Hkv, Nq, Tq, Nk, Tk, d, kv = _geometry_kv(q, k, cu_seqlens, max_seqlen, cu_seqlens_k,
                                                      max_seqlen_k, batch)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -291,6 +338,7 @@ def backward(q, k, v, o, dout, lse, causal=False, scale=None, cu_seqlens=None, m
              batch=None, deterministic=False, grad_dtype=torch.bfloat16, stream=None,
              workspace=None, check_status=False, cu_seqlens_k=None, max_seqlen_k=None):
     """Attention backward (preprocess + backward) through the C ABI; returns (dq, dk, dv)."""
+    _check_inputs(q, k, v, cu_seqlens, cu_seqlens_k, dout=dout, o=o, lse=lse)
     B, Hq, Hkv, Nq, Tq, Nk, Tk, d, kv = _geometry_kv(q, k, cu_seqlens, max_seqlen, cu_seqlens_k,
                                                      max_seqlen_k, batch)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)

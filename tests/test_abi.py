@@ -173,3 +173,22 @@ def test_product_package_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_tensor_api_rejects_bad_tensors():
+    """The tensor API checks dtype, rank, contiguity and device before any
+    library call (these run on CPU tensors: the checks come first)."""
+    import torch
+    q = torch.zeros(8, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="bfloat16"):
+        fa.forward(q.float(), q, q, batch=1)
+    with pytest.raises(ValueError, match="contiguous"):
+        fa.forward(q, q.transpose(0, 1).contiguous().transpose(0, 1), q, batch=1)
+    with pytest.raises(ValueError, match="dimensions"):
+        fa.forward(q[0], q, q, batch=1)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.forward(q, q, q, batch=1)
+    with pytest.raises(ValueError, match="multiple"):
+        fa.forward(torch.zeros(8, 3, 64, dtype=torch.bfloat16), q, q, batch=1)
+    with pytest.raises(ValueError, match="shape of q"):
+        fa.backward(q, q, q, q, q[:4], torch.zeros(2, 8), batch=1)
