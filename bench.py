@@ -37,6 +37,8 @@ if ROOT not in sys.path:
 import synth  # noqa: E402  (input generator: no attention arithmetic)
 
 METRIC = "attention fwd+bwd BF16 TFLOPs/s (hd128, causal) and % of GB300 dense BF16 peak"
+# --forward-only (head dimensions 192 and 256 have no backward)
+METRIC_FWD = "attention fwd BF16 TFLOPs/s and % of GB300 dense BF16 peak"
 
 # DRAM bytes (read + write) of one fa_bwd call -- the backward kernel and its
 # dQ conversion -- from an ncu capture (dram__bytes_read.sum +
@@ -231,6 +233,32 @@ def run_reference(args, w, inp, rank, world):
     return 0
 
 
+def report_forward_only(args, w, inp, world, rank, K, value, ms_per_step, fl_f, fwd_ms,
+                        launches_per_step, clocks, dist):
+    """JSON line of a --forward-only run: the forward's TFLOP/s and its roofline."""
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = fl_f / (fwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC_FWD, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded)", "config": config_of(w, inp, world),
+        "pct_of_nominal_peak": 100.0 * value / world / NOMINAL_PEAK_TFLOPS,
+        "pct_of_measured_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "kernel": "fa_fwd (scheduler + forward kernel)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} bf16 burst",
+                     "traffic": None},
+        "e2e": None, "gpu_launches": launches_per_step * K, "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -242,6 +270,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time the forward alone (no end-to-end leg, no CPU baseline)")
     ap.add_argument("--deterministic", action="store_true",
                     help="run the backward in deterministic mode whatever the workload's default")
     args = ap.parse_args()
@@ -312,6 +342,11 @@ def main():
                             scale, w.causal, cu, fws, fws_b, stream), "fa_fwd")
         if events:
             events[1].record(stream)
+        if args.forward_only:
+            if events:
+                events[2].record(stream)
+                events[3].record(stream)
+            return
         if kv:
             check(fa.fa_bwd_kv_preprocess(o, fa.FA_BF16, xi["dout"], Dv, bws, bws_b, B, Hq, Hkv, N,
                                           T, Nk, Tk, d, w.causal, cu, cu_k, det, stream),
@@ -332,12 +367,14 @@ def main():
         if events:
             events[3].record(stream)
 
-    launches_per_step = 6  # scheduler + fwd, scheduler + preprocess, bwd + postprocess
+    # scheduler + fwd, scheduler + preprocess, bwd + postprocess
+    launches_per_step = 2 if args.forward_only else 6
+    status_ws = fws if args.forward_only else bws
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    check(fa.fa_check_device_status(bws, stream), "device status")
+    check(fa.fa_check_device_status(status_ws, stream), "device status")
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
@@ -354,14 +391,19 @@ def main():
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    check(fa.fa_check_device_status(bws, stream), "device status")
+    check(fa.fa_check_device_status(status_ws, stream), "device status")
     t_fwd = [e[0].elapsed_time(e[1]) for e in evs]
     t_pre = [e[1].elapsed_time(e[2]) for e in evs]
     t_bwd = [e[2].elapsed_time(e[3]) for e in evs]
     t_step = [e[0].elapsed_time(e[3]) for e in evs]
     fl_f, fl_b = workload_flops(w, lengths, lengths_k)
+    if args.forward_only:
+        fl_b = 0.0
     value, total_ms = job_throughput((fl_f + fl_b) * K, sum(t_step), dist, dev)
     ms_per_step = total_ms / K
+    if args.forward_only:
+        return report_forward_only(args, w, inp, world, rank, K, value, ms_per_step, fl_f,
+                                   statistics.mean(t_fwd), launches_per_step, clocks, dist)
 
     # End to end through the public API with host buffers: every step copies
     # its inputs host -> device, runs fwd + bwd and copies the gradients back.

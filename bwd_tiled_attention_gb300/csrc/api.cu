@@ -108,7 +108,7 @@ fa_status check_shape(int B, int Hq, int Hkv, int Nq, int total_q, int Nk, int t
     if (B < 0 || Hq <= 0 || Hkv <= 0) return FA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if (Hq > kMaxHeads) return FA_ERR_UNSUPPORTED;
-    if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128 && d != 192 && d != 256) return FA_ERR_UNSUPPORTED;
     if ((cu_q == nullptr) != (cu_k == nullptr)) return FA_ERR_INVALID_ARG;
     s.B = B; s.Hq = Hq; s.Hkv = Hkv; s.Nq = Nq; s.Nk = Nk; s.d = d;
     s.varlen = cu_q != nullptr;
@@ -174,7 +174,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, fa_dtyp
     const int nsm = sm_count();
     if (nsm <= 0) return FA_ERR_CUDA;
     cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_sched(cu_q, B, Nq, s.Tq, Hq, kFwdBlockRows,
+    cudaError_t e = launch_sched(cu_q, B, Nq, s.Tq, Hq, d > 128 ? kFwdBlockRowsWide : kFwdBlockRows,
                                  causal ? kOrderLevelDesc : kOrderSeqDesc, lay.max_units,
                                  workspace, lay.units, 0, false, cu_k, Nk, s.Tk, strm);
     if (e != cudaSuccess) return FA_ERR_CUDA;
@@ -201,6 +201,7 @@ fa_status bwd_preprocess_impl(const void* o, fa_dtype o_dtype, const void* dout,
     Shape s;
     fa_status st = check_shape(B, Hq, Hkv, Nq, total_q, Nk, total_k, d, cu_q, cu_k, s);
     if (st != FA_OK) return st;
+    if (d > 128) return FA_ERR_UNSUPPORTED;  // the backward keeps 256 + 2d TMEM columns
     if (o_dtype != FA_BF16 && o_dtype != FA_FP32) return FA_ERR_INVALID_ARG;
     if (s.Tq == 0 || s.Tk == 0 || B == 0) return FA_OK;  // fa_bwd needs no workspace then
     if (!o || !dout || !D || !workspace) return FA_ERR_INVALID_ARG;
@@ -235,6 +236,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* dout
     Shape s;
     fa_status st = check_shape(B, Hq, Hkv, Nq, total_q, Nk, total_k, d, cu_q, cu_k, s);
     if (st != FA_OK) return st;
+    if (d > 128) return FA_ERR_UNSUPPORTED;  // the backward keeps 256 + 2d TMEM columns
     if (grad_dtype != FA_BF16 && grad_dtype != FA_FP32) return FA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_UNSUPPORTED;
     if (B == 0 || (s.Tq == 0 && s.Tk == 0)) return FA_OK;

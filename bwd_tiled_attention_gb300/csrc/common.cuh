@@ -12,6 +12,7 @@ namespace fa {
 
 constexpr int kTile = 128;          // rows of one query tile / key-value tile
 constexpr int kFwdBlockRows = 256;  // query rows of one forward work unit (two tiles)
+constexpr int kFwdBlockRowsWide = 128;  // the same for head dimensions above 128 (one tile)
 constexpr size_t kAlign = 256;      // alignment of every workspace segment
 
 // Device error word bits (workspace offset 0).
@@ -82,7 +83,7 @@ struct FwdWs {
 
 __host__ __device__ inline FwdWs fwd_ws_layout(int B, int Hq, int T) {
     FwdWs w;
-    w.max_units = max_tiles(B, T, kFwdBlockRows) * (long long)Hq;
+    w.max_units = max_tiles(B, T, kFwdBlockRowsWide) * (long long)Hq;  // any head dimension
     w.units = kAlign;
     w.bytes = align_up(w.units + (size_t)w.max_units * 8, kAlign);
     return w;

@@ -52,16 +52,21 @@ namespace {
 constexpr int kFwdThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+// D = 256 (head dimensions 192 and 256): one query tile per unit, since the
+// S and O columns of two tiles (2 x 128 + 2 x 256) exceed TMEM's 512, and one
+// K/V stage, since Q, K and V tiles are 64 KB each.
 template <int D>
 struct FwdCfg {
-    static constexpr int kStages = D == 128 ? 2 : 4;
-    static constexpr int kTileBytes = kTile * D * 2;  // one 128-row bf16 tile
-    static constexpr int kBoxes = D / 64;             // 64-column TMA boxes per tile
+    static constexpr int kStages = D == 256 ? 1 : (D == 128 ? 2 : 4);
+    static constexpr int kQTiles = D == 256 ? 1 : 2;   // query tiles per unit
+    static constexpr int kUnitRows = kQTiles * kTile;  // query rows per unit
+    static constexpr int kTileBytes = kTile * D * 2;   // one 128-row bf16 tile
+    static constexpr int kBoxes = D / 64;              // 64-column TMA boxes per tile
 };
 
 template <int D>
 struct FwdSmem {
-    alignas(1024) uint8_t q[2][FwdCfg<D>::kTileBytes];
+    alignas(1024) uint8_t q[FwdCfg<D>::kQTiles][FwdCfg<D>::kTileBytes];
     alignas(1024) uint8_t k[FwdCfg<D>::kStages][FwdCfg<D>::kTileBytes];
     alignas(1024) uint8_t v[FwdCfg<D>::kStages][FwdCfg<D>::kTileBytes];
     alignas(8) uint64_t sched_full[2], sched_empty[2];
@@ -75,7 +80,13 @@ struct FwdSmem {
     int zero;
 };
 
-// One work unit: query rows [256m, 256m + 256) of sequence b, head h.  t0/L
+// (the kernel aligns the dynamic shared memory to 1024 bytes itself)
+static_assert(sizeof(FwdSmem<64>) + 1024 <= 232448, "forward shared memory exceeds 227 KB");
+static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "forward shared memory exceeds 227 KB");
+static_assert(sizeof(FwdSmem<256>) + 1024 <= 232448, "forward shared memory exceeds 227 KB");
+
+// One work unit: query rows [Rm, Rm + R) of sequence b, head h (R = 256, or
+// 128 when D = 256).  t0/L
 // are the query tokens, tk0/Lk the key/value tokens; under the causal mask
 // query row r sees key c iff c <= r + Lk - L.  n[t] = key/value tiles query
 // tile t visits (0 when the tile is past the end, or sees no key at all).
@@ -85,7 +96,7 @@ struct UnitGeom {
 
 // KV = false: keys and queries share their boundaries (Lk = L, tk0 = t0), and
 // the geometry is the plain square one.
-template <bool KV>
+template <int D, bool KV>
 __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
     UnitGeom x;
     x.b = u.x;
@@ -99,11 +110,11 @@ __device__ __forceinline__ UnitGeom decode_unit(int2 u, const FwdParams& p) {
         x.tk0 = x.t0;
         x.Lk = x.L;
     }
-    const int r0 = x.m * kFwdBlockRows;
+    const int r0 = x.m * FwdCfg<D>::kUnitRows;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         const int rs = r0 + t * kTile;  // first row of tile t
-        if (rs >= x.L) {
+        if (t >= FwdCfg<D>::kQTiles || rs >= x.L) {
             x.n[t] = 0;
         } else if (p.causal) {
             const int re = min(rs + kTile, x.L);  // one past last valid row
@@ -246,8 +257,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 mbar_arrive(smem_u32(&sm.sched_full[slot]));
                 ++sched_it;
                 if (unit.x < 0) break;
-                const UnitGeom x = decode_unit<KV>(unit, p);
-                const int row0 = x.t0 + x.m * kFwdBlockRows;
+                const UnitGeom x = decode_unit<D, KV>(unit, p);
+                const int row0 = x.t0 + x.m * Cfg::kUnitRows;
                 if (!(ok = wait_or_abort(smem_u32(&sm.q_empty), (unit_it & 1) ^ 1, abort_flag, hdr)))
                     break;
                 // only the query tiles that see a key are loaded (none when no row of
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     mbar_arrive_expect_tx(qbar, (x.n[1] > 0 ? 2 : 1) * Cfg::kTileBytes);
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                    if (x.n[t] == 0) continue;
+                    if (t >= Cfg::kQTiles || x.n[t] == 0) continue;
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_3d(smem_u32(sm.q[t]) + c * 16384, &p.tm_q, qbar, c * 64, x.h,
                                     row0 + t * kTile);
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 mbar_arrive(smem_u32(&sm.sched_empty[slot]));
                 ++sched_it;
                 if (unit.x < 0) break;
-                const UnitGeom x = decode_unit<KV>(unit, p);
+                const UnitGeom x = decode_unit<D, KV>(unit, p);
                 if (!(ok = wait_or_abort(smem_u32(&sm.q_full), unit_it & 1, abort_flag, hdr)))
                     break;
                 for (int j = 0; j < x.nkv && ok; ++j) {
@@ -321,7 +332,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         if (!ok) break;
-                        if (j >= x.n[t]) continue;
+                        if (t >= Cfg::kQTiles || j >= x.n[t]) continue;
                         // S_t / P_t region is free once the previous O_t += P_t V is done
                         if (it[t] > 0 &&
                             !(ok = wait_or_abort(smem_u32(&sm.o_done[t]), (it[t] - 1) & 1,
@@ -344,7 +355,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         if (!ok) break;
-                        if (j >= x.n[t]) continue;
+                        if (t >= Cfg::kQTiles || j >= x.n[t]) continue;
                         if (!(ok = wait_or_abort(smem_u32(&sm.p_full[t]), it[t] & 1, abort_flag,
                                                  hdr)))
                             break;
@@ -396,17 +407,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
             ++sched_it;
             if (unit.x < 0) break;
-            const UnitGeom x = decode_unit<KV>(unit, p);
+            const UnitGeom x = decode_unit<D, KV>(unit, p);
             const int nt = t == 0 ? x.n[0] : x.n[1];
             if constexpr (!KV) {
                 if (nt == 0) continue;  // the tile is past the end
             }
-            const int r = x.m * kFwdBlockRows + t * kTile + row;  // row within the sequence
+            const int r = x.m * Cfg::kUnitRows + t * kTile + row;  // row within the sequence
             if constexpr (KV) {
                 if (nt == 0) {
                     // the tile is past the end, or none of its rows sees a key:
-                    // O = 0 and LSE = -inf, nothing on chip
-                    if (r < x.L) write_keyless_row<DR, OUT_FP32>(p, x.h, (size_t)x.t0 + (size_t)r);
+                    // O = 0 and LSE = -inf, nothing on chip.  (With one query tile
+                    // per unit, tile 1 is not a tile: its rows are the next unit's.)
+                    if (t < Cfg::kQTiles && r < x.L)
+                        write_keyless_row<DR, OUT_FP32>(p, x.h, (size_t)x.t0 + (size_t)r);
                     continue;
                 }
             }
@@ -561,7 +574,7 @@ cudaError_t launch_fwd_t(const FwdParams& p, int num_sms, cudaStream_t stream) {
     const size_t smem = sizeof(FwdSmem<D>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long long bound = max_tiles(p.B, p.T, kFwdBlockRows) * p.Hq;
+    const long long bound = max_tiles(p.B, p.T, FwdCfg<D>::kUnitRows) * p.Hq;
     const int grid = (int)(bound < num_sms ? bound : num_sms);
     if (grid <= 0) return cudaSuccess;
     return launch_pdl(kern, dim3(grid), dim3(kFwdThreads), smem, stream, p);
@@ -577,6 +590,12 @@ cudaError_t launch_fwd_kv(const FwdParams& p, int num_sms, cudaStream_t stream) 
     if (p.d == 96)
         return p.o_fp32 ? launch_fwd_t<128, 96, true, KV>(p, num_sms, stream)
                         : launch_fwd_t<128, 96, false, KV>(p, num_sms, stream);
+    if (p.d == 256)
+        return p.o_fp32 ? launch_fwd_t<256, 256, true, KV>(p, num_sms, stream)
+                        : launch_fwd_t<256, 256, false, KV>(p, num_sms, stream);
+    if (p.d == 192)
+        return p.o_fp32 ? launch_fwd_t<256, 192, true, KV>(p, num_sms, stream)
+                        : launch_fwd_t<256, 192, false, KV>(p, num_sms, stream);
     return p.o_fp32 ? launch_fwd_t<64, 64, true, KV>(p, num_sms, stream)
                     : launch_fwd_t<64, 64, false, KV>(p, num_sms, stream);
 }

@@ -32,11 +32,13 @@
  *   FA_ERR_INVALID_ARG by fa_check_device_status and produces no output).
  * - q, k, v, dout, dq, dk, dv and o must be 16-byte aligned (TMA).
  * - Query head h uses key/value head floor(h * Hkv / Hq); Hq % Hkv == 0.
- * - d must be 64, 96 or 128 (96 runs on 128-column tiles whose last 32
- *   columns are zero, at the tensor-core cost of d = 128).  Larger head
- *   dimensions return FA_ERR_UNSUPPORTED: the backward keeps S, dP, dK and
- *   dV of a tile in tensor memory (256 + 2d of its 512 columns) and the
- *   forward two query tiles' S and O (also 256 + 2d).  Inputs are bf16.
+ * - d must be 64, 96 or 128; the forward calls also take 192 and 256.
+ *   96 runs on 128-column tiles whose last 32 columns are zero (at the
+ *   tensor-core cost of d = 128), 192 likewise on 256-column tiles.  The
+ *   forward at 192 and 256 runs one 128-row query tile per work unit; the
+ *   backward calls return FA_ERR_UNSUPPORTED above 128, since they keep S,
+ *   dP, dK and dV of a tile in tensor memory (256 + 2d of its 512 columns).
+ *   Other head dimensions return FA_ERR_UNSUPPORTED.  Inputs are bf16.
  *   scale multiplies QK^T (usually
  *   1/sqrt(d)) and must be positive.  causal = 1 hides key j from query i
  *   when j > i (positions within the sequence; queries and keys have equal

@@ -65,6 +65,11 @@ def workloads() -> dict:
                                len_range=(256, 8192), deterministic=True),
         "mid_causal_d96": Workload("mid_causal_d96", B=4, Hq=16, Hkv=16, d=96, causal=True,
                                    seed=7, N=2048),
+        # forward only (bench.py --forward-only): the backward stops at d = 128
+        "mid_causal_d192": Workload("mid_causal_d192", B=4, Hq=16, Hkv=16, d=192, causal=True,
+                                    seed=8, N=2048),
+        "mid_causal_d256": Workload("mid_causal_d256", B=4, Hq=16, Hkv=16, d=256, causal=True,
+                                    seed=8, N=2048),
         **kv_workloads(),
     }
 

@@ -70,7 +70,7 @@ def fwd_call(**kw):
 
 def test_fwd_rejects_bad_arguments(L):
     assert fwd_call(Hkv=3) == fa.FA_ERR_INVALID_ARG            # Hq % Hkv != 0
-    assert fwd_call(d=256) == fa.FA_ERR_UNSUPPORTED             # head dim
+    assert fwd_call(d=512) == fa.FA_ERR_UNSUPPORTED             # head dim
     assert fwd_call(d=80) == fa.FA_ERR_UNSUPPORTED
     assert fwd_call(q=FAKE + 8) == fa.FA_ERR_INVALID_ARG        # TMA needs 16-byte alignment
     assert fwd_call(lse=None) == fa.FA_ERR_INVALID_ARG          # null output
@@ -103,6 +103,8 @@ def bwd_call(**kw):
 def test_bwd_rejects_bad_arguments(L):
     assert bwd_call(Hkv=3) == fa.FA_ERR_INVALID_ARG
     assert bwd_call(d=32) == fa.FA_ERR_UNSUPPORTED
+    assert bwd_call(d=256) == fa.FA_ERR_UNSUPPORTED             # forward-only head dims
+    assert bwd_call(d=192) == fa.FA_ERR_UNSUPPORTED
     assert bwd_call(dk=FAKE + 4) == fa.FA_ERR_INVALID_ARG
     assert bwd_call(D=None) == fa.FA_ERR_INVALID_ARG
     assert bwd_call(workspace_bytes=1024) == fa.FA_ERR_INVALID_ARG
@@ -133,7 +135,7 @@ def test_kv_calls_reject_bad_arguments(L):
     assert fwd_kv_call(cu_seqlens_k=FAKE, total_k=10) == fa.FA_ERR_INVALID_ARG
     assert fwd_kv_call(total_k=300) == fa.FA_ERR_INVALID_ARG    # dense Tk must be B*Nk
     assert fwd_kv_call(Nk=-1) == fa.FA_ERR_INVALID_ARG
-    assert fwd_kv_call(d=256) == fa.FA_ERR_UNSUPPORTED
+    assert fwd_kv_call(d=320) == fa.FA_ERR_UNSUPPORTED
     assert fwd_kv_call(k=FAKE + 8) == fa.FA_ERR_INVALID_ARG
     assert fwd_kv_call(Nq=0) == fa.FA_OK                        # no queries: nothing to do
     pre = dict(o=FAKE, o_dtype=fa.FA_BF16, dout=FAKE, D=FAKE, workspace=FAKE,
