@@ -44,7 +44,7 @@ METRIC_FWD = "attention fwd BF16 TFLOPs/s and % of GB300 dense BF16 peak"
 # dQ conversion -- from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum) of this bench's own command on the same workload,
 # for the kernels as they are; a workload without a capture reports null.
-FA_BWD_DRAM_BYTES = {"mid_causal": 775.6e6}
+FA_BWD_DRAM_BYTES = {"mid_causal": 775.6e6, "chunk_causal": 5188e6}
 NOMINAL_PEAK_TFLOPS = 2250.0
 
 
