@@ -194,3 +194,48 @@ def test_tensor_api_rejects_bad_tensors():
         fa.forward(torch.zeros(8, 3, 64, dtype=torch.bfloat16), q, q, batch=1)
     with pytest.raises(ValueError, match="shape of q"):
         fa.backward(q, q, q, q, q[:4], torch.zeros(2, 8), batch=1)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "fa.h"
+
+int main(void) {
+    /* status strings and workspace sizes need no GPU */
+    if (strcmp(fa_status_string(FA_ERR_TIMEOUT), "FA_ERR_TIMEOUT") != 0) return 1;
+    size_t f = fa_fwd_workspace_size(4, 16, 2048, 0);
+    size_t b = fa_bwd_workspace_size(4, 16, 16, 2048, 0, 128);
+    size_t bk = fa_bwd_kv_workspace_size(4, 16, 16, 2048, 0, 2048, 0, 128);
+    if (f == 0 || b == 0 || b != bk) return 2;
+    /* argument validation returns before any CUDA call */
+    void* p = (void*)(size_t)0x10000;
+    if (fa_fwd(p, p, p, p, FA_BF16, (float*)p, 2, 4, 3, 64, 0, 64, 0.125f, 1, NULL, p, 1 << 20,
+               NULL) != FA_ERR_INVALID_ARG) return 3;
+    if (fa_bwd(p, p, p, p, (const float*)p, (const float*)p, p, p, p, FA_BF16, p, 1 << 30, 2, 4,
+               2, 64, 0, 256, 0.1f, 0, NULL, 0, NULL) != FA_ERR_UNSUPPORTED) return 4;
+    printf("%s\n", fa_version());
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/fa.h compiles as C99 with warnings as errors, and a C program
+    linked against the library runs the calls that need no GPU."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    fabuild.build()
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    lib = fa.lib_path()
+    subprocess.check_call([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I",
+                           os.path.join(ROOT, "include"), str(src), "-o", str(exe), lib,
+                           "-Wl,-rpath," + os.path.dirname(lib)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    assert out.stdout.startswith("gb300")
