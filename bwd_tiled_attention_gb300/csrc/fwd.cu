@@ -72,6 +72,7 @@ struct FwdSmem {
     alignas(8) uint64_t sched_full[2], sched_empty[2];
     uint64_t q_full, q_empty;
     uint64_t k_full[FwdCfg<D>::kStages], v_full[FwdCfg<D>::kStages], kv_empty[FwdCfg<D>::kStages];
+    uint64_t k_empty1, v_empty1;  // one-stage ring (D = 256): K and V released separately
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
     uint64_t drain;
     int2 sched[2];
@@ -216,6 +217,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(smem_u32(&sm.v_full[s]), 1);
             mbar_init(smem_u32(&sm.kv_empty[s]), 1);
         }
+        if constexpr (S == 1) {
+            mbar_init(smem_u32(&sm.k_empty1), 1);
+            mbar_init(smem_u32(&sm.v_empty1), 1);
+        }
         mbar_init(smem_u32(&sm.drain), 1);
         sm.abort_flag = 0;
         sm.zero = 0;
@@ -279,14 +284,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 ++unit_it;
                 for (int j = 0; j < x.nkv && ok; ++j) {
                     const int st = kv_it % S;
-                    if (!(ok = wait_or_abort(smem_u32(&sm.kv_empty[st]), ((kv_it / S) & 1) ^ 1,
-                                             abort_flag, hdr)))
+                    // one stage: K(j) may land once S(j-1) is done, V(j) once PV(j-1) is
+                    const uint32_t k_free =
+                        smem_u32(S == 1 ? &sm.k_empty1 : &sm.kv_empty[st]);
+                    if (!(ok = wait_or_abort(k_free, ((kv_it / S) & 1) ^ 1, abort_flag, hdr)))
                         break;
                     const uint32_t kb = smem_u32(&sm.k_full[st]), vb = smem_u32(&sm.v_full[st]);
                     mbar_arrive_expect_tx(kb, Cfg::kTileBytes);
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_3d(smem_u32(sm.k[st]) + c * 16384, &p.tm_k, kb, c * 64, x.g,
                                     x.tk0 + j * kTile);
+                    if constexpr (S == 1) {
+                        if (!(ok = wait_or_abort(smem_u32(&sm.v_empty1), (kv_it & 1) ^ 1,
+                                                 abort_flag, hdr)))
+                            break;
+                    }
                     mbar_arrive_expect_tx(vb, Cfg::kTileBytes);
                     for (int c = 0; c < Cfg::kBoxes; ++c)
                         tma_load_3d(smem_u32(sm.v[st]) + c * 16384, &p.tm_v, vb, c * 64, x.g,
@@ -351,6 +363,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     if (!ok) break;
                     // the unit's last S MMAs are issued: Q may be overwritten once they finish
                     if (j == x.nkv - 1) mma_commit(smem_u32(&sm.q_empty));
+                    if constexpr (S == 1) mma_commit(smem_u32(&sm.k_empty1));  // K read by S
                     if (!(ok = wait_or_abort(smem_u32(&sm.v_full[st]), par, abort_flag, hdr))) break;
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
@@ -374,7 +387,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         mma_commit(smem_u32(&sm.o_done[t]));
                         ++it[t];
                     }
-                    mma_commit(smem_u32(&sm.kv_empty[st]));
+                    if constexpr (S == 1)
+                        mma_commit(smem_u32(&sm.v_empty1));  // V read by PV
+                    else
+                        mma_commit(smem_u32(&sm.kv_empty[st]));
                     ++kv_it;
                 }
                 if (!ok) break;
