@@ -52,13 +52,13 @@ namespace {
 constexpr int kFwdThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// D = 256 (head dimensions 192 and 256): one query tile per unit, since the
-// S and O columns of two tiles (2 x 128 + 2 x 256) exceed TMEM's 512, and one
-// K/V stage, since Q, K and V tiles are 64 KB each.
+// D = 192 and 256: one query tile per unit, since the S and O columns of two
+// tiles (2 x 128 + 2 x D) exceed TMEM's 512, and one K/V stage, since Q, K and
+// V tiles are 48 or 64 KB each.
 template <int D>
 struct FwdCfg {
-    static constexpr int kStages = D == 256 ? 1 : (D == 128 ? 2 : 4);
-    static constexpr int kQTiles = D == 256 ? 1 : 2;   // query tiles per unit
+    static constexpr int kStages = D > 128 ? 1 : (D == 128 ? 2 : 4);
+    static constexpr int kQTiles = D > 128 ? 1 : 2;    // query tiles per unit
     static constexpr int kUnitRows = kQTiles * kTile;  // query rows per unit
     static constexpr int kTileBytes = kTile * D * 2;   // one 128-row bf16 tile
     static constexpr int kBoxes = D / 64;              // 64-column TMA boxes per tile
@@ -84,6 +84,7 @@ struct FwdSmem {
 // (the kernel aligns the dynamic shared memory to 1024 bytes itself)
 static_assert(sizeof(FwdSmem<64>) + 1024 <= 232448, "forward shared memory exceeds 227 KB");
 static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "forward shared memory exceeds 227 KB");
+static_assert(sizeof(FwdSmem<192>) + 1024 <= 232448, "forward shared memory exceeds 227 KB");
 static_assert(sizeof(FwdSmem<256>) + 1024 <= 232448, "forward shared memory exceeds 227 KB");
 
 // One work unit: query rows [Rm, Rm + R) of sequence b, head h (R = 256, or
@@ -610,8 +611,8 @@ cudaError_t launch_fwd_kv(const FwdParams& p, int num_sms, cudaStream_t stream) 
         return p.o_fp32 ? launch_fwd_t<256, 256, true, KV>(p, num_sms, stream)
                         : launch_fwd_t<256, 256, false, KV>(p, num_sms, stream);
     if (p.d == 192)
-        return p.o_fp32 ? launch_fwd_t<256, 192, true, KV>(p, num_sms, stream)
-                        : launch_fwd_t<256, 192, false, KV>(p, num_sms, stream);
+        return p.o_fp32 ? launch_fwd_t<192, 192, true, KV>(p, num_sms, stream)
+                        : launch_fwd_t<192, 192, false, KV>(p, num_sms, stream);
     return p.o_fp32 ? launch_fwd_t<64, 64, true, KV>(p, num_sms, stream)
                     : launch_fwd_t<64, 64, false, KV>(p, num_sms, stream);
 }

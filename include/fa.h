@@ -34,8 +34,8 @@
  * - Query head h uses key/value head floor(h * Hkv / Hq); Hq % Hkv == 0.
  * - d must be 64, 96 or 128; the forward calls also take 192 and 256.
  *   96 runs on 128-column tiles whose last 32 columns are zero (at the
- *   tensor-core cost of d = 128), 192 likewise on 256-column tiles.  The
- *   forward at 192 and 256 runs one 128-row query tile per work unit; the
+ *   tensor-core cost of d = 128).  The forward at 192 and 256 runs one
+ *   128-row query tile per work unit; the
  *   backward calls return FA_ERR_UNSUPPORTED above 128, since they keep S,
  *   dP, dK and dV of a tile in tensor memory (256 + 2d of its 512 columns).
  *   Other head dimensions return FA_ERR_UNSUPPORTED.  Inputs are bf16.

@@ -1,8 +1,7 @@
 """Forward parity for head dimensions 192 and 256 (forward only: the backward
 returns FA_ERR_UNSUPPORTED above 128), against the fp64 oracle.
 
-These run one 128-row query tile per work unit with 256-column tiles; d = 192
-is zero-padded to 256.  Cases: packed varlen with ragged tails, GQA and MQA,
+These run one 128-row query tile per work unit on 192- or 256-column tiles.  Cases: packed varlen with ragged tails, GQA and MQA,
 causal and not, different query and key lengths, fp32 O."""
 import numpy as np
 import pytest
