@@ -63,6 +63,8 @@ def workloads() -> dict:
                                N=8192),
         "varlen_det": Workload("varlen_det", B=16, Hq=16, Hkv=16, d=128, causal=True, seed=4,
                                len_range=(256, 8192), deterministic=True),
+        "mid_causal_d64": Workload("mid_causal_d64", B=4, Hq=16, Hkv=16, d=64, causal=True,
+                                   seed=7, N=2048),
         "mid_causal_d96": Workload("mid_causal_d96", B=4, Hq=16, Hkv=16, d=96, causal=True,
                                    seed=7, N=2048),
         # forward only (bench.py --forward-only): the backward stops at d = 128
