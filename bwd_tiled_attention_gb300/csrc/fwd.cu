@@ -25,7 +25,10 @@
 // feeds two MMAs, and the tensor core works on one tile while the softmax
 // warps of the other tile run.  TMEM: S_0 [0,128), S_1 [128,256), O_0
 // [256,256+d), O_1 [384,384+d); P_t is written as bf16 over the first 64
-// columns of S_t.
+// columns of S_t.  Head dimensions above 128 leave room for one query tile
+// (O takes [256,256+d)); its S is then double-buffered over [0,256): S(j+1)
+// is issued before O += P(j) V, so the tensor core computes the next scores
+// while the softmax warps work on the current ones (warps 8..11 idle).
 //
 // Softmax uses exp2 with the scale folded in (s * scale * log2 e), packed
 // fp32-pair arithmetic for the scale and the row sum, and 3-input maxima.  All
@@ -72,13 +75,17 @@ struct FwdSmem {
     alignas(8) uint64_t sched_full[2], sched_empty[2];
     uint64_t q_full, q_empty;
     uint64_t k_full[FwdCfg<D>::kStages], v_full[FwdCfg<D>::kStages], kv_empty[FwdCfg<D>::kStages];
-    uint64_t k_empty1, v_empty1;  // one-stage ring (D = 256): K and V released separately
+    uint64_t k_empty1, v_empty1;  // one stage (D > 128): K and V released separately
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
     uint64_t drain;
     int2 sched[2];
     uint32_t tmem_base;
     int abort_flag;
     int zero;
+    // D > 128: the last unit's row statistics, from the softmax warps to the
+    // epilogue warps
+    float ep_m[D > 128 ? kTile : 1], ep_l[D > 128 ? kTile : 1];
+    uint64_t ep_full;
 };
 
 // (the kernel aligns the dynamic shared memory to 1024 bytes itself)
@@ -184,6 +191,47 @@ __device__ __forceinline__ void write_keyless_row(const FwdParams& p, int h, siz
     }
 }
 
+// Epilogue of one row: O = O~ / l and LSE = (m + log2 l) * ln 2, O~ read from
+// TMEM columns [o_addr, o_addr + DR).  Only a valid row is stored; every thread
+// of the warp takes part in the TMEM loads.
+template <int DR, bool OUT_FP32, bool KV>
+__device__ __forceinline__ void store_row(const FwdParams& p, uint32_t o_addr, int h, size_t tok,
+                                          bool valid, float m_ref, float l) {
+    // l = 0 only for a KV row that sees no key
+    const float inv_l = KV ? (l > 0.f ? 1.f / l : 0.f) : 1.f / l;
+    if (valid) p.lse[(size_t)h * p.T + tok] = (m_ref + __log2f(l)) * 0.69314718055994531f;
+#pragma unroll 1
+    for (int c = 0; c < DR / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(o_addr + c * 32, ov);
+        tmem_ld_wait();
+        if (valid) {
+            const size_t base = (tok * p.Hq + h) * DR + c * 32;
+            if (OUT_FP32) {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l,
+                                         __uint_as_float(ov[4 * i + 1]) * inv_l,
+                                         __uint_as_float(ov[4 * i + 2]) * inv_l,
+                                         __uint_as_float(ov[4 * i + 3]) * inv_l);
+            } else {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + base);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pack_bf16x2(__uint_as_float(ov[8 * i]) * inv_l,
+                                                    __uint_as_float(ov[8 * i + 1]) * inv_l),
+                                        pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv_l,
+                                                    __uint_as_float(ov[8 * i + 3]) * inv_l),
+                                        pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv_l,
+                                                    __uint_as_float(ov[8 * i + 5]) * inv_l),
+                                        pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv_l,
+                                                    __uint_as_float(ov[8 * i + 7]) * inv_l));
+            }
+        }
+    }
+}
+
 // D: the tile layout (64 or 128 columns); DR: the head dimension in memory.
 // DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros,
 // which add nothing to S, and O's last 32 columns (all zero) are not stored.
@@ -223,6 +271,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(smem_u32(&sm.v_empty1), 1);
         }
         mbar_init(smem_u32(&sm.drain), 1);
+        if constexpr (D > 128) mbar_init(smem_u32(&sm.ep_full), kTile);
         sm.abort_flag = 0;
         sm.zero = 0;
         fence_barrier_init();
@@ -251,6 +300,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
             int sched_it = 0, kv_it = 0, unit_it = 0;
+            int k_it = 0, v_it = 0;  // D > 128: K and V loads, counted apart
             bool ok = true;
             while (ok) {
                 const int slot = sched_it & 1;
@@ -283,33 +333,61 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                     row0 + t * kTile);
                 }
                 ++unit_it;
-                for (int j = 0; j < x.nkv && ok; ++j) {
-                    const int st = kv_it % S;
-                    // one stage: K(j) may land once S(j-1) is done, V(j) once PV(j-1) is
-                    const uint32_t k_free =
-                        smem_u32(S == 1 ? &sm.k_empty1 : &sm.kv_empty[st]);
-                    if (!(ok = wait_or_abort(k_free, ((kv_it / S) & 1) ^ 1, abort_flag, hdr)))
-                        break;
-                    const uint32_t kb = smem_u32(&sm.k_full[st]), vb = smem_u32(&sm.v_full[st]);
-                    mbar_arrive_expect_tx(kb, Cfg::kTileBytes);
-                    for (int c = 0; c < Cfg::kBoxes; ++c)
-                        tma_load_3d(smem_u32(sm.k[st]) + c * 16384, &p.tm_k, kb, c * 64, x.g,
-                                    x.tk0 + j * kTile);
-                    if constexpr (S == 1) {
-                        if (!(ok = wait_or_abort(smem_u32(&sm.v_empty1), (kv_it & 1) ^ 1,
+                if constexpr (D > 128) {
+                    // K runs one tile ahead of V, in the order the MMA thread
+                    // consumes them (S(j+1) is issued before PV(j)): iteration j
+                    // loads K(j) once S(j-1) has read the K stage, then V(j-1)
+                    // once PV(j-2) has read the V stage.
+                    for (int j = 0; j <= x.nkv && ok; ++j) {
+                        if (j < x.nkv) {
+                            if (!(ok = wait_or_abort(smem_u32(&sm.k_empty1), (k_it & 1) ^ 1,
+                                                     abort_flag, hdr)))
+                                break;
+                            const uint32_t kb = smem_u32(&sm.k_full[0]);
+                            mbar_arrive_expect_tx(kb, Cfg::kTileBytes);
+                            for (int c = 0; c < Cfg::kBoxes; ++c)
+                                tma_load_3d(smem_u32(sm.k[0]) + c * 16384, &p.tm_k, kb, c * 64,
+                                            x.g, x.tk0 + j * kTile);
+                            ++k_it;
+                        }
+                        if (j >= 1) {
+                            if (!(ok = wait_or_abort(smem_u32(&sm.v_empty1), (v_it & 1) ^ 1,
+                                                     abort_flag, hdr)))
+                                break;
+                            const uint32_t vb = smem_u32(&sm.v_full[0]);
+                            mbar_arrive_expect_tx(vb, Cfg::kTileBytes);
+                            for (int c = 0; c < Cfg::kBoxes; ++c)
+                                tma_load_3d(smem_u32(sm.v[0]) + c * 16384, &p.tm_v, vb, c * 64,
+                                            x.g, x.tk0 + (j - 1) * kTile);
+                            ++v_it;
+                        }
+                    }
+                } else {
+                    for (int j = 0; j < x.nkv && ok; ++j) {
+                        const int st = kv_it % S;
+                        if (!(ok = wait_or_abort(smem_u32(&sm.kv_empty[st]), ((kv_it / S) & 1) ^ 1,
                                                  abort_flag, hdr)))
                             break;
+                        const uint32_t kb = smem_u32(&sm.k_full[st]), vb = smem_u32(&sm.v_full[st]);
+                        mbar_arrive_expect_tx(kb, Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kBoxes; ++c)
+                            tma_load_3d(smem_u32(sm.k[st]) + c * 16384, &p.tm_k, kb, c * 64, x.g,
+                                        x.tk0 + j * kTile);
+                        mbar_arrive_expect_tx(vb, Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kBoxes; ++c)
+                            tma_load_3d(smem_u32(sm.v[st]) + c * 16384, &p.tm_v, vb, c * 64, x.g,
+                                        x.tk0 + j * kTile);
+                        ++kv_it;
                     }
-                    mbar_arrive_expect_tx(vb, Cfg::kTileBytes);
-                    for (int c = 0; c < Cfg::kBoxes; ++c)
-                        tma_load_3d(smem_u32(sm.v[st]) + c * 16384, &p.tm_v, vb, c * 64, x.g,
-                                    x.tk0 + j * kTile);
-                    ++kv_it;
                 }
             }
             // Never leave a TMA write in flight: wait (bounded) for the last
             // phase armed on every load barrier.
             const volatile int* z = &sm.zero;
+            if constexpr (D > 128) {
+                if (k_it > 0) mbar_wait(smem_u32(&sm.k_full[0]), (k_it - 1) & 1, z);
+                if (v_it > 0) mbar_wait(smem_u32(&sm.v_full[0]), (v_it - 1) & 1, z);
+            }
             for (int i = 0; i < S && i < kv_it; ++i) {
                 const int it = kv_it - 1 - i, st = it % S, par = (it / S) & 1;
                 mbar_wait(smem_u32(&sm.k_full[st]), par, z);
@@ -326,6 +404,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             int sched_it = 0, kv_it = 0, unit_it = 0;
             int it[2] = {0, 0};   // PV MMAs issued per tile (= softmax iterations)
             int ep[2] = {0, 0};   // units whose epilogue must finish before O_t is reused
+            int g = 0, k_it = 0, v_it = 0;  // D > 128: S/PV steps, K and V tiles consumed
             bool ok = true;
             while (ok) {
                 const int slot = sched_it & 1;
@@ -339,65 +418,127 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const UnitGeom x = decode_unit<D, KV>(unit, p);
                 if (!(ok = wait_or_abort(smem_u32(&sm.q_full), unit_it & 1, abort_flag, hdr)))
                     break;
-                for (int j = 0; j < x.nkv && ok; ++j) {
-                    const int st = kv_it % S, par = (kv_it / S) & 1;
-                    if (!(ok = wait_or_abort(smem_u32(&sm.k_full[st]), par, abort_flag, hdr))) break;
+                if constexpr (D > 128) {
+                    // One query tile, S double-buffered: step g (counted over all
+                    // units) computes S into columns [128 (g & 1), +128), and S(j+1)
+                    // is issued before PV(j), so the tensor core computes the next
+                    // scores while the softmax warps work on the current ones.
+                    // Iteration j issues S(j), then PV(j-1).
+                    const int n = x.n[0];
+                    for (int j = 0; j <= x.nkv && ok; ++j) {
+                        if (j < x.nkv) {
+                            if (!(ok = wait_or_abort(smem_u32(&sm.k_full[0]), k_it & 1, abort_flag,
+                                                     hdr)))
+                                break;
+                            if (j < n) {
+                                const int gj = g + j, b = gj & 1;
+                                // the buffer is free once PV(gj - 2) has read its P
+                                if (gj >= 2 &&
+                                    !(ok = wait_or_abort(smem_u32(&sm.o_done[b]), ((gj - 2) >> 1) & 1,
+                                                         abort_flag, hdr)))
+                                    break;
+                                tc_fence_after();
+                                const uint32_t qa = smem_u32(sm.q[0]), kb = smem_u32(sm.k[0]);
 #pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        if (!ok) break;
-                        if (t >= Cfg::kQTiles || j >= x.n[t]) continue;
-                        // S_t / P_t region is free once the previous O_t += P_t V is done
-                        if (it[t] > 0 &&
-                            !(ok = wait_or_abort(smem_u32(&sm.o_done[t]), (it[t] - 1) & 1,
-                                                 abort_flag, hdr)))
-                            break;
-                        tc_fence_after();
-                        const uint32_t qa = smem_u32(sm.q[t]), kb = smem_u32(sm.k[st]);
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(tmem + t * 128, make_sdesc(qa + off, 16, 1024),
-                                   make_sdesc(kb + off, 16, 1024), idS, kk > 0);
+                                for (int kk = 0; kk < D / 16; ++kk) {
+                                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                    mma_ss(tmem + b * 128, make_sdesc(qa + off, 16, 1024),
+                                           make_sdesc(kb + off, 16, 1024), idS, kk > 0);
+                                }
+                                mma_commit(smem_u32(&sm.s_full[b]));
+                            }
+                            if (j == x.nkv - 1) mma_commit(smem_u32(&sm.q_empty));
+                            mma_commit(smem_u32(&sm.k_empty1));
+                            ++k_it;
                         }
-                        mma_commit(smem_u32(&sm.s_full[t]));
+                        if (j >= 1) {
+                            const int jp = j - 1;
+                            if (!(ok = wait_or_abort(smem_u32(&sm.v_full[0]), v_it & 1, abort_flag,
+                                                     hdr)))
+                                break;
+                            if (jp < n) {
+                                const int gj = g + jp, b = gj & 1;
+                                if (!(ok = wait_or_abort(smem_u32(&sm.p_full[b]), (gj >> 1) & 1,
+                                                         abort_flag, hdr)))
+                                    break;
+                                if (jp == 0 && ep[0] > 0 &&
+                                    !(ok = wait_or_abort(smem_u32(&sm.o_free[0]), (ep[0] - 1) & 1,
+                                                         abort_flag, hdr)))
+                                    break;
+                                tc_fence_after();
+                                const uint32_t vb = smem_u32(sm.v[0]);
+#pragma unroll
+                                for (int kk = 0; kk < kTile / 16; ++kk)
+                                    mma_ts(tmem + 256, tmem + b * 128 + kk * 8,
+                                           make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
+                                           (jp > 0 || kk > 0) ? 1u : 0u);
+                                mma_commit(smem_u32(&sm.o_done[b]));
+                            }
+                            mma_commit(smem_u32(&sm.v_empty1));
+                            ++v_it;
+                        }
                     }
                     if (!ok) break;
-                    // the unit's last S MMAs are issued: Q may be overwritten once they finish
-                    if (j == x.nkv - 1) mma_commit(smem_u32(&sm.q_empty));
-                    if constexpr (S == 1) mma_commit(smem_u32(&sm.k_empty1));  // K read by S
-                    if (!(ok = wait_or_abort(smem_u32(&sm.v_full[st]), par, abort_flag, hdr))) break;
+                    g += n;
+                    ++unit_it;
+                    ep[0] += n > 0;
+                } else {
+                    for (int j = 0; j < x.nkv && ok; ++j) {
+                        const int st = kv_it % S, par = (kv_it / S) & 1;
+                        if (!(ok = wait_or_abort(smem_u32(&sm.k_full[st]), par, abort_flag, hdr))) break;
 #pragma unroll
-                    for (int t = 0; t < 2; ++t) {
+                        for (int t = 0; t < 2; ++t) {
+                            if (!ok) break;
+                            if (t >= Cfg::kQTiles || j >= x.n[t]) continue;
+                            // S_t / P_t region is free once the previous O_t += P_t V is done
+                            if (it[t] > 0 &&
+                                !(ok = wait_or_abort(smem_u32(&sm.o_done[t]), (it[t] - 1) & 1,
+                                                     abort_flag, hdr)))
+                                break;
+                            tc_fence_after();
+                            const uint32_t qa = smem_u32(sm.q[t]), kb = smem_u32(sm.k[st]);
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                mma_ss(tmem + t * 128, make_sdesc(qa + off, 16, 1024),
+                                       make_sdesc(kb + off, 16, 1024), idS, kk > 0);
+                            }
+                            mma_commit(smem_u32(&sm.s_full[t]));
+                        }
                         if (!ok) break;
-                        if (t >= Cfg::kQTiles || j >= x.n[t]) continue;
-                        if (!(ok = wait_or_abort(smem_u32(&sm.p_full[t]), it[t] & 1, abort_flag,
-                                                 hdr)))
-                            break;
-                        if (j == 0 && ep[t] > 0 &&
-                            !(ok = wait_or_abort(smem_u32(&sm.o_free[t]), (ep[t] - 1) & 1,
-                                                 abort_flag, hdr)))
-                            break;
-                        tc_fence_after();
-                        const uint32_t vb = smem_u32(sm.v[st]);
-                        const uint32_t o_col = 256 + t * 128, p_col = t * 128;
+                        // the unit's last S MMAs are issued: Q may be overwritten once they finish
+                        if (j == x.nkv - 1) mma_commit(smem_u32(&sm.q_empty));
+                        if (!(ok = wait_or_abort(smem_u32(&sm.v_full[st]), par, abort_flag, hdr))) break;
 #pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ts(tmem + o_col, tmem + p_col + kk * 8,
-                                   make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(smem_u32(&sm.o_done[t]));
-                        ++it[t];
-                    }
-                    if constexpr (S == 1)
-                        mma_commit(smem_u32(&sm.v_empty1));  // V read by PV
-                    else
+                        for (int t = 0; t < 2; ++t) {
+                            if (!ok) break;
+                            if (t >= Cfg::kQTiles || j >= x.n[t]) continue;
+                            if (!(ok = wait_or_abort(smem_u32(&sm.p_full[t]), it[t] & 1, abort_flag,
+                                                     hdr)))
+                                break;
+                            if (j == 0 && ep[t] > 0 &&
+                                !(ok = wait_or_abort(smem_u32(&sm.o_free[t]), (ep[t] - 1) & 1,
+                                                     abort_flag, hdr)))
+                                break;
+                            tc_fence_after();
+                            const uint32_t vb = smem_u32(sm.v[st]);
+                            const uint32_t o_col = 256 + t * 128, p_col = t * 128;
+#pragma unroll
+                            for (int kk = 0; kk < kTile / 16; ++kk)
+                                mma_ts(tmem + o_col, tmem + p_col + kk * 8,
+                                       make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                            mma_commit(smem_u32(&sm.o_done[t]));
+                            ++it[t];
+                        }
                         mma_commit(smem_u32(&sm.kv_empty[st]));
-                    ++kv_it;
-                }
-                if (!ok) break;
-                ++unit_it;
+                        ++kv_it;
+                    }
+                    if (!ok) break;
+                    ++unit_it;
 #pragma unroll
-                for (int t = 0; t < 2; ++t) ep[t] += x.n[t] > 0;
+                    for (int t = 0; t < 2; ++t) ep[t] += x.n[t] > 0;
+                }
             }
             // all issued MMAs complete before TMEM is released
             mma_commit(smem_u32(&sm.drain));
@@ -411,8 +552,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int row = q4 * 32 + lane;         // row within the tile
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + t * 128;
-        const uint32_t o_addr = tmem + lane_off + 256 + t * 128;
+        // (D > 128: one O, stored by warps 8..11)
+        const uint32_t o_addr = tmem + lane_off + 256 + (D > 128 ? 0 : t * 128);
         int sched_it = 0, it = 0;
+        int ue = 0;  // D > 128: units handed from the softmax to the epilogue warps
         bool ok = true;
         while (ok) {
             const int slot = sched_it & 1;
@@ -425,6 +568,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ++sched_it;
             if (unit.x < 0) break;
             const UnitGeom x = decode_unit<D, KV>(unit, p);
+            if constexpr (D > 128) {
+                if (t == 1) {
+                    // Epilogue warps: store the unit the softmax warps have finished
+                    // while those go on with the next one.  it counts the unit's
+                    // steps as the softmax warps do, so the last PV is step it - 1.
+                    if (x.n[0] == 0) continue;
+                    it += x.n[0];
+                    if (!(ok = warp_wait(smem_u32(&sm.ep_full), ue & 1, abort_flag, hdr))) break;
+                    if (!(ok = warp_wait(smem_u32(&sm.o_done[(it - 1) & 1]), ((it - 1) >> 1) & 1,
+                                         abort_flag, hdr)))
+                        break;
+                    tc_fence_after();
+                    ++ue;
+                    const int r = x.m * kTile + row;
+                    store_row<DR, OUT_FP32, KV>(p, o_addr, x.h, (size_t)x.t0 + (size_t)r, r < x.L,
+                                                sm.ep_m[row], sm.ep_l[row]);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sm.o_free[0]));
+                    continue;
+                }
+            }
             const int nt = t == 0 ? x.n[0] : x.n[1];
             if constexpr (!KV) {
                 if (nt == 0) continue;  // the tile is past the end
@@ -445,16 +610,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                  : (p.causal ? min(r + 1, x.L) : x.L);
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < nt; ++j) {
-                if (!(ok = warp_wait(smem_u32(&sm.s_full[t]), it & 1, abort_flag, hdr))) break;
+                // D > 128: S alternates between two buffers, step by step
+                const int buf = D > 128 ? (it & 1) : t;
+                const uint32_t s_at = D > 128 ? s_addr + (uint32_t)buf * 128 : s_addr;
+                if (!(ok = warp_wait(smem_u32(&sm.s_full[buf]), D > 128 ? (it >> 1) & 1 : it & 1,
+                                     abort_flag, hdr)))
+                    break;
                 tc_fence_after();
                 float s[128];
                 {
                     // all four 32-column loads in flight, one wait
                     uint32_t r0[32], r1[32], r2[32], r3[32];
-                    tmem_ld32(s_addr, r0);
-                    tmem_ld32(s_addr + 32, r1);
-                    tmem_ld32(s_addr + 64, r2);
-                    tmem_ld32(s_addr + 96, r3);
+                    tmem_ld32(s_at, r0);
+                    tmem_ld32(s_at + 32, r1);
+                    tmem_ld32(s_at + 64, r2);
+                    tmem_ld32(s_at + 96, r3);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -498,7 +668,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
                     softmax_chunk(s + c * 32, p.scale_log2, neg, acc, pk);
-                    tmem_st16(s_addr + c * 16, pk);
+                    tmem_st16(s_at + c * 16, pk);
                 }
                 {
                     float a0, a1, b0, b1;
@@ -507,7 +677,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     l += (a0 + a1) + (b0 + b1);
                 }
                 if (__any_sync(0xffffffffu, need)) {
-                    // O~ is stable here: S_t(j) was committed after O_t += P_t V of j-1.
+                    // O~ must be stable.  Two query tiles: S_t(j) was committed after
+                    // O_t += P_t V of j-1.  One tile (D > 128): S(j) may finish first,
+                    // so wait for PV(j-1) (j >= 1 whenever a rescale is needed).
+                    if constexpr (D > 128) {
+                        if (!(ok = warp_wait(smem_u32(&sm.o_done[(it - 1) & 1]), ((it - 1) >> 1) & 1,
+                                             abort_flag, hdr)))
+                            break;
+                        tc_fence_after();
+                    }
 #pragma unroll 1
                     for (int c = 0; c < DR / 32; ++c) {
                         uint32_t ov[32];
@@ -526,49 +704,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[t]));
+                if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[buf]));
                 ++it;
             }
             if (!ok) break;
+            if constexpr (D > 128) {
+                // hand m and l to the epilogue warps, once they have read the
+                // previous unit's
+                if (ue > 0 &&
+                    !(ok = warp_wait(smem_u32(&sm.o_free[0]), (ue - 1) & 1, abort_flag, hdr)))
+                    break;
+                sm.ep_m[row] = m_ref;
+                sm.ep_l[row] = l;
+                mbar_arrive(smem_u32(&sm.ep_full));
+                ++ue;
+                continue;
+            }
             // epilogue: O = O~ / l, LSE = (m + log2 l) * ln 2
             if (!(ok = warp_wait(smem_u32(&sm.o_done[t]), (it - 1) & 1, abort_flag, hdr))) break;
             tc_fence_after();
-            const bool valid = r < x.L;
-            // l = 0 only for a KV row that sees no key
-            const float inv_l = KV ? (l > 0.f ? 1.f / l : 0.f) : 1.f / l;
-            const size_t tok = (size_t)x.t0 + (size_t)r;
-            if (valid) p.lse[(size_t)x.h * p.T + tok] = (m_ref + __log2f(l)) * 0.69314718055994531f;
-#pragma unroll 1
-            for (int c = 0; c < DR / 32; ++c) {
-                uint32_t ov[32];
-                tmem_ld32(o_addr + c * 32, ov);
-                tmem_ld_wait();
-                if (valid) {
-                    const size_t base = (tok * p.Hq + x.h) * DR + c * 32;
-                    if (OUT_FP32) {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + base);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l,
-                                                 __uint_as_float(ov[4 * i + 1]) * inv_l,
-                                                 __uint_as_float(ov[4 * i + 2]) * inv_l,
-                                                 __uint_as_float(ov[4 * i + 3]) * inv_l);
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + base);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(
-                                pack_bf16x2(__uint_as_float(ov[8 * i]) * inv_l,
-                                            __uint_as_float(ov[8 * i + 1]) * inv_l),
-                                pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv_l,
-                                            __uint_as_float(ov[8 * i + 3]) * inv_l),
-                                pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv_l,
-                                            __uint_as_float(ov[8 * i + 5]) * inv_l),
-                                pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv_l,
-                                            __uint_as_float(ov[8 * i + 7]) * inv_l));
-                    }
-                }
-            }
+            store_row<DR, OUT_FP32, KV>(p, o_addr, x.h, (size_t)x.t0 + (size_t)r, r < x.L, m_ref, l);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.o_free[t]));

@@ -155,3 +155,41 @@ def test_mid_dense_deterministic():
                         scale=w.scale, batch=w.B, deterministic=True, check_status=True)
         for a, b_ in zip(ref, g):
             assert torch.equal(a.view(torch.int16), b_.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["mid_causal_d192", "mid_causal_d256"])
+def test_wide_head_forward_full(name):
+    """Forward at head dimensions 192 and 256 on the benchmark's workload: 1024
+    one-tile units on 152 CTAs, so every CTA walks several units and the two
+    score buffers alternate across unit boundaries.  Whole heads and sampled
+    rows against the oracle, in bf16 and fp32 O; repeats are bit-identical
+    (every unit writes only its own rows)."""
+    w = synth.workloads()[name]
+    inp = synth.make_workload(w)
+    x = cuda_inputs(inp)
+    oi = oracle_inputs(inp)
+    cu = inp["cu_seqlens"].numpy()
+    rng = np.random.default_rng(7)
+    for out_dtype in (torch.bfloat16, torch.float32):
+        o, lse = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, batch=w.B,
+                            out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        stored = out_dtype == torch.bfloat16
+        for b, h in ((0, 0), (3, 15)):
+            s0, s1 = int(cu[b]), int(cu[b + 1])
+            sl = lambda a: a[s0:s1, h:h + 1]
+            ref = oracle.attention(sl(oi["q"]), sl(oi["k"]), sl(oi["v"]), [0, s1 - s0], w.scale,
+                                   w.causal)
+            assert_close(f"o b{b} h{h}", to_np(o[s0:s1, h]), ref["o"][:, 0], stored_bf16=stored)
+            assert_lse(to_np(lse[h, s0:s1]), ref["lse"][0])
+        for b, h in ((1, 7), (2, 3)):
+            L = int(cu[b + 1] - cu[b])
+            rows = np.unique(np.concatenate([[0, L - 1], rng.integers(0, L, 24)]))
+            ref = oracle.rows(oi["q"], oi["k"], oi["v"], cu, w.scale, w.causal, b, h, rows)
+            t = cu[b] + rows
+            assert_close(f"o b{b} h{h}", to_np(o[t, h]), ref["o"], stored_bf16=stored)
+            assert_lse(to_np(lse[h, t]), ref["lse"])
+        for _ in range(2):
+            o2, lse2 = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale,
+                                  batch=w.B, out_dtype=out_dtype)
+            assert torch.equal(o, o2) and torch.equal(lse, lse2)

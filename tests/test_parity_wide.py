@@ -1,8 +1,10 @@
 """Forward parity for head dimensions 192 and 256 (forward only: the backward
 returns FA_ERR_UNSUPPORTED above 128), against the fp64 oracle.
 
-These run one 128-row query tile per work unit on 192- or 256-column tiles.  Cases: packed varlen with ragged tails, GQA and MQA,
-causal and not, different query and key lengths, fp32 O."""
+These run one 128-row query tile per work unit on 192- or 256-column tiles.
+Cases: packed varlen with ragged tails, GQA and MQA, causal and not,
+different query and key lengths (including rows that see no key), more units
+than CTAs, fp32 O."""
 import numpy as np
 import pytest
 import torch
@@ -28,6 +30,10 @@ def assert_lse_kv(got, ref, tol=1e-3):
     (192, 6, 1, [257, 64, 500], None),
     (256, 2, 2, [100, 300], [400, 300]),
     (192, 4, 4, [300, 77], [129, 600]),
+    # more units than CTAs, so CTAs walk several units: with Lq > Lk the first
+    # query tiles of a sequence see no key (dummy steps between real ones)
+    (256, 24, 4, [600, 333, 900], [200, 333, 1000]),
+    (192, 16, 2, [700, 1000, 520, 900], None),
 ])
 def test_wide_head_forward(d, Hq, Hkv, lq, lk, causal):
     kv = lk is not None
