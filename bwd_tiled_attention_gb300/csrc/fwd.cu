@@ -56,8 +56,12 @@ constexpr int kFwdThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // D = 192 and 256: one query tile per unit, since the S and O columns of two
-// tiles (2 x 128 + 2 x D) exceed TMEM's 512, and one K/V stage, since Q, K and
-// V tiles are 48 or 64 KB each.
+// tiles (2 x 128 + 2 x D) exceed TMEM's 512, and one K stage, since Q, K and V
+// tiles are 48 or 64 KB each.  V has a ring of its own in the room left: V(j)
+// is split into chunks of kVChunk columns (PV runs per chunk, N = kVChunk),
+// over kVSlots slots -- d = 256: halves of 128 columns in 3 slots of 32 KB;
+// d = 192: whole tiles in 2 slots of 48 KB.  Up to 128 the V ring is the K/V
+// ring: kStages slots of whole tiles.
 template <int D>
 struct FwdCfg {
     static constexpr int kStages = D > 128 ? 1 : (D == 128 ? 2 : 4);
@@ -65,17 +69,23 @@ struct FwdCfg {
     static constexpr int kUnitRows = kQTiles * kTile;  // query rows per unit
     static constexpr int kTileBytes = kTile * D * 2;   // one 128-row bf16 tile
     static constexpr int kBoxes = D / 64;              // 64-column TMA boxes per tile
+    static constexpr int kVChunk = D == 256 ? 128 : D;                   // V columns per chunk
+    static constexpr int kVChunks = D / kVChunk;                         // chunks per V tile
+    static constexpr int kVSlots = D == 256 ? 3 : (D > 128 ? 2 : kStages);
+    static constexpr int kVSlotBytes = kTile * kVChunk * 2;
+    static_assert(kVChunks * kVChunk == D && kVChunk % 64 == 0, "V chunks must tile the row");
 };
 
 template <int D>
 struct FwdSmem {
     alignas(1024) uint8_t q[FwdCfg<D>::kQTiles][FwdCfg<D>::kTileBytes];
     alignas(1024) uint8_t k[FwdCfg<D>::kStages][FwdCfg<D>::kTileBytes];
-    alignas(1024) uint8_t v[FwdCfg<D>::kStages][FwdCfg<D>::kTileBytes];
+    alignas(1024) uint8_t v[FwdCfg<D>::kVSlots][FwdCfg<D>::kVSlotBytes];
     alignas(8) uint64_t sched_full[2], sched_empty[2];
     uint64_t q_full, q_empty;
-    uint64_t k_full[FwdCfg<D>::kStages], v_full[FwdCfg<D>::kStages], kv_empty[FwdCfg<D>::kStages];
-    uint64_t k_empty1, v_empty1;  // one stage (D > 128): K and V released separately
+    uint64_t k_full[FwdCfg<D>::kStages], v_full[FwdCfg<D>::kVSlots], kv_empty[FwdCfg<D>::kStages];
+    // D > 128: K and the V slots are released separately
+    uint64_t k_empty1, v_empty[D > 128 ? FwdCfg<D>::kVSlots : 1];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
     uint64_t drain;
     int2 sched[2];
@@ -263,12 +273,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_init(smem_u32(&sm.q_empty), 1);
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&sm.k_full[s]), 1);
-            mbar_init(smem_u32(&sm.v_full[s]), 1);
             mbar_init(smem_u32(&sm.kv_empty[s]), 1);
         }
-        if constexpr (S == 1) {
+        for (int s = 0; s < Cfg::kVSlots; ++s) mbar_init(smem_u32(&sm.v_full[s]), 1);
+        if constexpr (D > 128) {
             mbar_init(smem_u32(&sm.k_empty1), 1);
-            mbar_init(smem_u32(&sm.v_empty1), 1);
+            for (int s = 0; s < Cfg::kVSlots; ++s) mbar_init(smem_u32(&sm.v_empty[s]), 1);
         }
         mbar_init(smem_u32(&sm.drain), 1);
         if constexpr (D > 128) mbar_init(smem_u32(&sm.ep_full), kTile);
@@ -300,7 +310,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
             int sched_it = 0, kv_it = 0, unit_it = 0;
-            int k_it = 0, v_it = 0;  // D > 128: K and V loads, counted apart
+            int k_it = 0, v_it = 0;  // D > 128: K tiles and V chunks loaded
             bool ok = true;
             while (ok) {
                 const int slot = sched_it & 1;
@@ -336,8 +346,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if constexpr (D > 128) {
                     // K runs one tile ahead of V, in the order the MMA thread
                     // consumes them (S(j+1) is issued before PV(j)): iteration j
-                    // loads K(j) once S(j-1) has read the K stage, then V(j-1)
-                    // once PV(j-2) has read the V stage.
+                    // loads K(j) once S(j-1) has read the K stage, then the chunks
+                    // of V(j-1), each once its slot's previous chunk has been read.
                     for (int j = 0; j <= x.nkv && ok; ++j) {
                         if (j < x.nkv) {
                             if (!(ok = wait_or_abort(smem_u32(&sm.k_empty1), (k_it & 1) ^ 1,
@@ -350,15 +360,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                             x.g, x.tk0 + j * kTile);
                             ++k_it;
                         }
-                        if (j >= 1) {
-                            if (!(ok = wait_or_abort(smem_u32(&sm.v_empty1), (v_it & 1) ^ 1,
-                                                     abort_flag, hdr)))
+                        for (int h = 0; j >= 1 && h < Cfg::kVChunks && ok; ++h) {
+                            const int slot = v_it % Cfg::kVSlots;
+                            if (!(ok = wait_or_abort(smem_u32(&sm.v_empty[slot]),
+                                                     ((v_it / Cfg::kVSlots) & 1) ^ 1, abort_flag,
+                                                     hdr)))
                                 break;
-                            const uint32_t vb = smem_u32(&sm.v_full[0]);
-                            mbar_arrive_expect_tx(vb, Cfg::kTileBytes);
-                            for (int c = 0; c < Cfg::kBoxes; ++c)
-                                tma_load_3d(smem_u32(sm.v[0]) + c * 16384, &p.tm_v, vb, c * 64,
-                                            x.g, x.tk0 + (j - 1) * kTile);
+                            const uint32_t vb = smem_u32(&sm.v_full[slot]);
+                            mbar_arrive_expect_tx(vb, Cfg::kVSlotBytes);
+                            for (int c = 0; c < Cfg::kVChunk / 64; ++c)
+                                tma_load_3d(smem_u32(sm.v[slot]) + c * 16384, &p.tm_v, vb,
+                                            h * Cfg::kVChunk + c * 64, x.g, x.tk0 + (j - 1) * kTile);
                             ++v_it;
                         }
                     }
@@ -386,7 +398,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const volatile int* z = &sm.zero;
             if constexpr (D > 128) {
                 if (k_it > 0) mbar_wait(smem_u32(&sm.k_full[0]), (k_it - 1) & 1, z);
-                if (v_it > 0) mbar_wait(smem_u32(&sm.v_full[0]), (v_it - 1) & 1, z);
+                for (int i = 0; i < Cfg::kVSlots && i < v_it; ++i) {
+                    const int it = v_it - 1 - i;
+                    mbar_wait(smem_u32(&sm.v_full[it % Cfg::kVSlots]), (it / Cfg::kVSlots) & 1, z);
+                }
             }
             for (int i = 0; i < S && i < kv_it; ++i) {
                 const int it = kv_it - 1 - i, st = it % S, par = (it / S) & 1;
@@ -400,11 +415,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         setmaxnreg_dec<72>();
         if (lane == 0) {
             constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idPV = make_idesc_bf16(128, D, false, true);
+            constexpr uint32_t idPV = make_idesc_bf16(128, Cfg::kVChunk, false, true);
             int sched_it = 0, kv_it = 0, unit_it = 0;
             int it[2] = {0, 0};   // PV MMAs issued per tile (= softmax iterations)
             int ep[2] = {0, 0};   // units whose epilogue must finish before O_t is reused
-            int g = 0, k_it = 0, v_it = 0;  // D > 128: S/PV steps, K and V tiles consumed
+            int g = 0, k_it = 0, v_it = 0;  // D > 128: S/PV steps, K tiles and V chunks consumed
             bool ok = true;
             while (ok) {
                 const int slot = sched_it & 1;
@@ -452,12 +467,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             ++k_it;
                         }
                         if (j >= 1) {
-                            const int jp = j - 1;
-                            if (!(ok = wait_or_abort(smem_u32(&sm.v_full[0]), v_it & 1, abort_flag,
-                                                     hdr)))
-                                break;
+                            // PV(j-1), chunk by chunk of V columns, each V slot
+                            // released once its chunk has been read
+                            const int jp = j - 1, gj = g + jp, b = gj & 1;
                             if (jp < n) {
-                                const int gj = g + jp, b = gj & 1;
                                 if (!(ok = wait_or_abort(smem_u32(&sm.p_full[b]), (gj >> 1) & 1,
                                                          abort_flag, hdr)))
                                     break;
@@ -465,17 +478,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                     !(ok = wait_or_abort(smem_u32(&sm.o_free[0]), (ep[0] - 1) & 1,
                                                          abort_flag, hdr)))
                                     break;
-                                tc_fence_after();
-                                const uint32_t vb = smem_u32(sm.v[0]);
-#pragma unroll
-                                for (int kk = 0; kk < kTile / 16; ++kk)
-                                    mma_ts(tmem + 256, tmem + b * 128 + kk * 8,
-                                           make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
-                                           (jp > 0 || kk > 0) ? 1u : 0u);
-                                mma_commit(smem_u32(&sm.o_done[b]));
                             }
-                            mma_commit(smem_u32(&sm.v_empty1));
-                            ++v_it;
+                            for (int h = 0; h < Cfg::kVChunks; ++h) {
+                                const int slot = v_it % Cfg::kVSlots;
+                                if (!(ok = wait_or_abort(smem_u32(&sm.v_full[slot]),
+                                                         (v_it / Cfg::kVSlots) & 1, abort_flag, hdr)))
+                                    break;
+                                if (jp < n) {
+                                    tc_fence_after();
+                                    const uint32_t vb = smem_u32(sm.v[slot]);
+#pragma unroll
+                                    for (int kk = 0; kk < kTile / 16; ++kk)
+                                        mma_ts(tmem + 256 + h * Cfg::kVChunk, tmem + b * 128 + kk * 8,
+                                               make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
+                                               (jp > 0 || kk > 0) ? 1u : 0u);
+                                }
+                                mma_commit(smem_u32(&sm.v_empty[slot]));
+                                ++v_it;
+                            }
+                            if (!ok) break;
+                            if (jp < n) mma_commit(smem_u32(&sm.o_done[b]));
                         }
                     }
                     if (!ok) break;
