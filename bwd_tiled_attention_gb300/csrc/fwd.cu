@@ -28,7 +28,8 @@
 // columns of S_t.  Head dimensions above 128 leave room for one query tile
 // (O takes [256,256+d)); its S is then double-buffered over [0,256): S(j+1)
 // is issued before O += P(j) V, so the tensor core computes the next scores
-// while the softmax warps work on the current ones (warps 8..11 idle).
+// while the softmax warps work on the current ones, and warps 8..11 store O.
+// At d = 192, P has the last 64 columns to itself.
 //
 // Softmax uses exp2 with the scale folded in (s * scale * log2 e), packed
 // fp32-pair arithmetic for the scale and the row sum, and 3-input maxima.  All
@@ -73,7 +74,12 @@ struct FwdCfg {
     static constexpr int kVChunks = D / kVChunk;                         // chunks per V tile
     static constexpr int kVSlots = D == 256 ? 3 : (D > 128 ? 2 : kStages);
     static constexpr int kVSlotBytes = kTile * kVChunk * 2;
+    // d = 192 leaves 64 TMEM columns past O: P gets them to itself instead of
+    // being written over its S buffer, so the next S need not wait for PV.
+    static constexpr bool kSepP = D > 128 && 256 + D + 64 <= 512;
+    static constexpr int kPCol = 256 + D;  // first column of P when kSepP
     static_assert(kVChunks * kVChunk == D && kVChunk % 64 == 0, "V chunks must tile the row");
+    static_assert(!kSepP || kPCol + 64 <= 512, "P past the TMEM columns");
 };
 
 template <int D>
@@ -447,8 +453,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                 break;
                             if (j < n) {
                                 const int gj = g + j, b = gj & 1;
-                                // the buffer is free once PV(gj - 2) has read its P
-                                if (gj >= 2 &&
+                                // The buffer's last scores, S(gj - 2), were read by the
+                                // softmax before PV(gj - 2) was issued; with P written
+                                // over them it is free once PV(gj - 2) has read P too.
+                                if (!Cfg::kSepP && gj >= 2 &&
                                     !(ok = wait_or_abort(smem_u32(&sm.o_done[b]), ((gj - 2) >> 1) & 1,
                                                          abort_flag, hdr)))
                                     break;
@@ -489,7 +497,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                     const uint32_t vb = smem_u32(sm.v[slot]);
 #pragma unroll
                                     for (int kk = 0; kk < kTile / 16; ++kk)
-                                        mma_ts(tmem + 256 + h * Cfg::kVChunk, tmem + b * 128 + kk * 8,
+                                        mma_ts(tmem + 256 + h * Cfg::kVChunk,
+                                               tmem + (Cfg::kSepP ? Cfg::kPCol : b * 128) + kk * 8,
                                                make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
                                                (jp > 0 || kk > 0) ? 1u : 0u);
                                 }
@@ -686,11 +695,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
                 const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
                 uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+                if constexpr (Cfg::kSepP) {
+                    // P has a region of its own: compute it in registers, then store
+                    // it once PV(it - 1) has read the previous P (which also makes
+                    // O~ stable for the rescale below)
+                    uint32_t pk[4][16];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-                    softmax_chunk(s + c * 32, p.scale_log2, neg, acc, pk);
-                    tmem_st16(s_at + c * 16, pk);
+                    for (int c = 0; c < 4; ++c) softmax_chunk(s + c * 32, p.scale_log2, neg, acc, pk[c]);
+                    if (it > 0 && !(ok = warp_wait(smem_u32(&sm.o_done[(it - 1) & 1]),
+                                                   ((it - 1) >> 1) & 1, abort_flag, hdr)))
+                        break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_st16(tmem + lane_off + Cfg::kPCol + c * 16, pk[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16];
+                        softmax_chunk(s + c * 32, p.scale_log2, neg, acc, pk);
+                        tmem_st16(s_at + c * 16, pk);
+                    }
                 }
                 {
                     float a0, a1, b0, b1;
@@ -702,7 +726,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     // O~ must be stable.  Two query tiles: S_t(j) was committed after
                     // O_t += P_t V of j-1.  One tile (D > 128): S(j) may finish first,
                     // so wait for PV(j-1) (j >= 1 whenever a rescale is needed).
-                    if constexpr (D > 128) {
+                    if constexpr (D > 128 && !Cfg::kSepP) {
                         if (!(ok = warp_wait(smem_u32(&sm.o_done[(it - 1) & 1]), ((it - 1) >> 1) & 1,
                                              abort_flag, hdr)))
                             break;
