@@ -20,7 +20,7 @@
 //                read from TMEM
 //   warp 2       TMEM allocation
 //   warps 4..7   softmax for query tile 0 (one thread per row)
-//   warps 8..11  softmax for query tile 1
+//   warps 8..11  softmax for query tile 1 (above d = 128: the epilogue)
 // A unit covers 256 query rows (two 128-row tiles) so each K/V tile loaded
 // feeds two MMAs, and the tensor core works on one tile while the softmax
 // warps of the other tile run.  TMEM: S_0 [0,128), S_1 [128,256), O_0
@@ -111,7 +111,7 @@ static_assert(sizeof(FwdSmem<192>) + 1024 <= 232448, "forward shared memory exce
 static_assert(sizeof(FwdSmem<256>) + 1024 <= 232448, "forward shared memory exceeds 227 KB");
 
 // One work unit: query rows [Rm, Rm + R) of sequence b, head h (R = 256, or
-// 128 when D = 256).  t0/L
+// 128 when D > 128).  t0/L
 // are the query tokens, tk0/Lk the key/value tokens; under the causal mask
 // query row r sees key c iff c <= r + Lk - L.  n[t] = key/value tiles query
 // tile t visits (0 when the tile is past the end, or sees no key at all).
@@ -248,7 +248,8 @@ __device__ __forceinline__ void store_row(const FwdParams& p, uint32_t o_addr, i
     }
 }
 
-// D: the tile layout (64 or 128 columns); DR: the head dimension in memory.
+// D: the tile layout (64, 128, 192 or 256 columns); DR: the head dimension in
+// memory.
 // DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros,
 // which add nothing to S, and O's last 32 columns (all zero) are not stored.
 template <int D, int DR, bool OUT_FP32, bool KV>
