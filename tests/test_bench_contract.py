@@ -1,0 +1,52 @@
+"""The benchmark's reference arm on CPU: `bench.py --impl reference` times the
+fp64 oracle on a bounded sample of the workload and prints one JSON line with
+the same metric, unit and config as the GPU arm; under torchrun only rank 0
+prints it, and the other ranks exit 0 without work."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(extra_env=None):
+    env = dict(os.environ, **(extra_env or {}))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--ref-step-s", "0.5"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_reference_arm_line():
+    lines = _run()
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    import bench
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 0
+    assert d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert d["config"]["workload"].startswith("mid_causal:")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["unit"] == "TFLOP/s" and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    # ms_per_step is the workload's FLOPs at the measured rate
+    fl = sum(bench.workload_flops(*_workload_args()))
+    assert abs(d["ms_per_step"] - fl / (d["value"] * 1e12) * 1e3) <= 1e-6 * d["ms_per_step"]
+
+
+def _workload_args():
+    import synth
+    w = synth.workloads()["mid_causal"]
+    inp = synth.make_workload(w)
+    return w, inp["lengths"], inp.get("lengths_k")
+
+
+def test_reference_arm_other_rank_is_silent():
+    assert _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
