@@ -587,6 +587,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                 }
                 if (!ok) break;
+                if constexpr (KV) {
+                    // A unit that no query sees issues no dV, whose first one waits
+                    // for the previous unit's dK/dV epilogue.  Wait for it here, or
+                    // two such units in a row could put dkv_full two phases ahead of
+                    // the epilogue warps, which parity cannot tell apart.
+                    if (x.ni == 0 && unit_it > 0 &&
+                        !(ok = wait_or_abort(smem_u32(&sm.dkv_free), (unit_it - 1) & 1, abort_flag,
+                                             hdr)))
+                        break;
+                }
                 mma_commit(smem_u32(&sm.dkv_full));
                 mma_commit(smem_u32(&sm.kv_empty));
                 ++unit_it;

@@ -5,8 +5,8 @@ positions of the key sequence: query i sees key j iff j <= i + Lk - Lq.
 Small packed batches are compared element by element: shorter and longer key
 sequences, ragged tails, a single query, more queries than keys (rows that
 see no key: O = 0, LSE = -inf, dQ = 0), empty query or key sequences (dK =
-dV = 0 for keys no query sees), GQA/MQA and both head dims, atomic and
-deterministic.  The full-size chunk workload (2048 new tokens against 8192
+dV = 0 for keys no query sees, also in long runs of such units per CTA),
+GQA/MQA and three head dims, atomic and deterministic.  The full-size chunk workload (2048 new tokens against 8192
 keys) is checked on sampled rows and keys, and must be bit-identical over
 repeats in deterministic mode."""
 import numpy as np
@@ -27,6 +27,9 @@ CASES = [
     ("d64_mqa", [256, 100, 5], [700, 100, 383], 6, 1, 64),
     ("empty_sides", [0, 50, 128, 0], [200, 0, 128, 0], 2, 2, 128),
     ("d96", [129, 300], [700, 300], 4, 2, 96),
+    # ~1500 key/value units that no query sees, about ten in a row per CTA,
+    # between ordinary ones: their dK/dV hand-offs must keep in step
+    ("many_keyless_units", [0, 300, 0, 129], [8192, 400, 4096, 129], 16, 4, 128),
 ]
 
 
