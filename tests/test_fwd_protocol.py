@@ -28,6 +28,12 @@ Layouts modelled:
 - d = 192: as d = 256 but with whole V tiles over 2 slots and P in TMEM
   columns of its own.
 
+The one-tile model also runs its softmax and epilogue warpgroups as four
+warps each, each arriving on its own and owning a quarter of the rows. Each
+arrival carries the step or unit it stands for, and a phase that completes
+with arrivals for two different ones is a hazard: a fast warp must never
+arrive for its next step inside the phase its neighbours are completing.
+
 Planted mistakes in each protocol must be caught, so the checks have teeth.
 """
 import random
@@ -42,9 +48,16 @@ class Hazard(Exception):
 class Barrier:
     def __init__(self, count):
         self.count, self.arrived, self.tx, self.phases = count, 0, 0, 0
+        self.tags = set()
 
-    def arrive(self):
+    def arrive(self, tag=None):
+        """tag: what the arrival stands for (a step, a unit); one phase must not
+        mix arrivals for different ones."""
         self.arrived += 1
+        if tag is not None:
+            self.tags.add(tag)
+            if len(self.tags) > 1:
+                raise Hazard(f"one phase mixes arrivals for {sorted(self.tags)}")
         self._complete()
 
     def expect_tx(self, tx):
@@ -59,6 +72,7 @@ class Barrier:
         if self.arrived == self.count and self.tx == 0:
             self.phases += 1
             self.arrived = 0
+            self.tags = set()
 
 
 class Sim:
@@ -353,21 +367,26 @@ def test_two_tile_planted_mistakes(mistake):
 
 # ------------------------------------------------------------------ d > 128
 
-def run_one_tile(units, seed, nv, slots, sep_p, mistake=None):
+def run_one_tile(units, seed, nv, slots, sep_p, mistake=None, warps=1):
     """units: list of (n, nkv): steps with MMAs (0: no row sees a key), and
-    key/value tiles loaded (>= 1)."""
-    sim = Sim(units, seed, consumers=3)  # MMA issuer + softmax + epilogue warps
+    key/value tiles loaded (>= 1).  warps: the softmax and the epilogue
+    warpgroups as one actor each (1), or as four warps arriving on their own
+    (4), each owning a quarter of the rows."""
+    sim = Sim(units, seed, consumers=1 + 2 * warps)  # MMA issuer + softmax + epilogue warps
     for i in (0, 1):
-        for name in ("s_full", "p_full", "o_done"):
-            sim.bar(f"{name}{i}")
-    for name in ("o_free", "q_full", "q_empty", "k_full", "k_empty", "ep_full"):
+        sim.bar(f"s_full{i}")
+        sim.bar(f"o_done{i}")
+        sim.bar(f"p_full{i}", warps)
+    for name in ("q_full", "q_empty", "k_full", "k_empty"):
         sim.bar(name)
+    for name in ("o_free", "ep_full"):
+        sim.bar(name, warps)
     for i in range(slots):
         sim.bar(f"v_full{i}")
         sim.bar(f"v_empty{i}")
     smem = {}
     st = {"v_read": {}, "S": {}, "S_read": {}, "P": {}, "O": [[] for _ in range(nv)],
-          "stats": None}
+          "stats": {}}
 
     def producer():
         it_sched = it_unit = k_it = v_it = 0
@@ -452,7 +471,7 @@ def run_one_tile(units, seed, nv, slots, sep_p, mistake=None):
             it_unit += 1
             ep += n > 0
 
-    def softmax():
+    def softmax(w):
         it_sched = it = ue = 0
         while True:
             unit = yield from sim.take(it_sched)
@@ -461,39 +480,41 @@ def run_one_tile(units, seed, nv, slots, sep_p, mistake=None):
                 return
             uid, n, _ = unit
             if n == 0:
-                sim.out.append(("keyless", uid))
+                if w == 0:
+                    sim.out.append(("keyless", uid))
                 continue
             for j in range(n):
                 b = it & 1
                 while not sim.ready(f"s_full{b}", (it >> 1) & 1, (it >> 1) + 1):
                     yield
                 if st["S"].get(b) != (uid, j):
-                    raise Hazard(f"softmax ({uid},{j}) read S{b} = {st['S'].get(b)}")
+                    raise Hazard(f"softmax warp {w} ({uid},{j}) read S{b} = {st['S'].get(b)}")
                 yield  # the exponentials
                 if st["S"].get(b) != (uid, j):
                     raise Hazard("S overwritten while the softmax read it")
-                st["S_read"][b] = True
+                st["S_read"].setdefault(b, set()).add(w)
                 rescale = j > 0 and sim.rnd.random() < 0.3
                 if (sep_p or rescale) and it >= 1 and mistake != "no_pv_wait":
                     while not sim.ready(f"o_done{(it - 1) & 1}", ((it - 1) >> 1) & 1, ((it - 1) >> 1) + 1):
                         yield
                 p_at = "sep" if sep_p else b
-                if st["P"].get(p_at) not in (None, "read"):
-                    raise Hazard(f"P ({uid},{j}) written over unread P {st['P'][p_at]}")
-                st["P"][p_at] = (uid, j)
+                mine = st["P"].setdefault(p_at, {})
+                if mine.get(w) not in (None, "read"):
+                    raise Hazard(f"P ({uid},{j}) of warp {w} written over unread P {mine[w]}")
+                mine[w] = (uid, j)
                 if rescale and any(o != [(uid, q) for q in range(j)] for o in st["O"]):
                     raise Hazard(f"rescale of ({uid},{j}) saw O = {st['O']}")
-                sim.bars[f"p_full{b}"].arrive()
+                sim.bars[f"p_full{b}"].arrive((uid, j))
                 it += 1
                 yield
             if ue > 0 and mistake != "no_stats_wait":
                 while not sim.ready("o_free", (ue - 1) & 1, ue):
                     yield
-            st["stats"] = uid
-            sim.bars["ep_full"].arrive()
+            st["stats"][w] = uid
+            sim.bars["ep_full"].arrive(uid)
             ue += 1
 
-    def epilogue():
+    def epilogue(w):
         it_sched = it = ue = 0
         while True:
             unit = yield from sim.take(it_sched)
@@ -509,14 +530,15 @@ def run_one_tile(units, seed, nv, slots, sep_p, mistake=None):
             while not sim.ready(f"o_done{(it - 1) & 1}", ((it - 1) >> 1) & 1, ((it - 1) >> 1) + 1):
                 yield
             ue += 1
-            for _ in range(2):  # reads O and the statistics over a while
-                if st["stats"] != uid:
-                    raise Hazard(f"epilogue of {uid} read the statistics of {st['stats']}")
+            for _ in range(2):  # reads O and the statistics of its rows over a while
+                if st["stats"].get(w) != uid:
+                    raise Hazard(f"epilogue warp {w} of {uid} read the statistics of {st['stats'].get(w)}")
                 if any(o != [(uid, q) for q in range(n)] for o in st["O"]):
                     raise Hazard(f"epilogue of {uid} read O = {st['O']}")
                 yield
-            sim.out.append(("stored", uid))
-            sim.bars["o_free"].arrive()
+            if w == 0:
+                sim.out.append(("stored", uid))
+            sim.bars["o_free"].arrive(uid)
 
     def execute(op, arg):
         if op == "commit":
@@ -527,26 +549,30 @@ def run_one_tile(units, seed, nv, slots, sep_p, mistake=None):
             uid, j, b = arg
             if smem.get("q") != uid or smem.get("k") != (uid, j):
                 raise Hazard(f"S ({uid},{j}) read Q {smem.get('q')}, K {smem.get('k')}")
-            if st["S_read"].get(b) is False:
+            if b in st["S"] and len(st["S_read"].get(b, ())) < warps:
                 raise Hazard(f"S ({uid},{j}) overwrote unread scores {st['S'][b]}")
-            if not sep_p and st["P"].get(b) not in (None, "read"):
+            if not sep_p and any(v != "read" for v in st["P"].get(b, {}).values()):
                 raise Hazard(f"S ({uid},{j}) overwrote P {st['P'][b]} before PV read it")
-            st["S"][b], st["S_read"][b] = (uid, j), False
+            st["S"][b], st["S_read"][b] = (uid, j), set()
             if not sep_p:
-                st["P"][b] = None
+                st["P"][b] = {}
         elif op == "PV":
             uid, j, b, h, s = arg
             p_at = "sep" if sep_p else b
-            if smem.get(f"v{s}") != (uid, j, h) or st["P"].get(p_at) != (uid, j):
-                raise Hazard(f"PV ({uid},{j},{h}) read V {smem.get(f'v{s}')}, P {st['P'].get(p_at)}")
+            quarters = st["P"].get(p_at, {})
+            if smem.get(f"v{s}") != (uid, j, h) or len(quarters) != warps or any(
+                    v != (uid, j) for v in quarters.values()):
+                raise Hazard(f"PV ({uid},{j},{h}) read V {smem.get(f'v{s}')}, P {quarters}")
             if j == 0:
                 st["O"][h] = []
             st["O"][h].append((uid, j))
             st["v_read"][s] = True
             if h == nv - 1:
-                st["P"][p_at] = "read"
+                st["P"][p_at] = {w: "read" for w in quarters}
 
-    sim.run([producer(), mma(), softmax(), epilogue()], execute, smem)
+    roles = [producer(), mma()] + [softmax(w) for w in range(warps)] + [
+        epilogue(w) for w in range(warps)]
+    sim.run(roles, execute, smem)
     check_outputs(sim, [(u, units[u][0] == 0) for u in range(len(units))])
 
 
@@ -563,10 +589,12 @@ def random_one_tile_units(rnd):
 ONE_TILE = {"d256": dict(nv=2, slots=3, sep_p=False), "d192": dict(nv=1, slots=2, sep_p=True)}
 
 
+@pytest.mark.parametrize("warps", [1, 4])
 @pytest.mark.parametrize("cfg", sorted(ONE_TILE))
-def test_one_tile_protocol_is_hazard_and_deadlock_free(cfg):
-    for seed in range(400):
-        run_one_tile(random_one_tile_units(random.Random(seed * 7 + 1)), seed, **ONE_TILE[cfg])
+def test_one_tile_protocol_is_hazard_and_deadlock_free(cfg, warps):
+    for seed in range(400 if warps == 1 else 200):
+        run_one_tile(random_one_tile_units(random.Random(seed * 7 + 1)), seed, warps=warps,
+                     **ONE_TILE[cfg])
 
 
 # As above; no_s_buffer_wait is implied by an in-order tensor pipe (S(j)
@@ -576,16 +604,17 @@ ONE_TILE_MISTAKES = {"no_s_buffer_wait": False, "no_v_slot_wait": True, "no_pv_w
                      "no_stats_wait": True, "no_o_free_wait": True}
 
 
+@pytest.mark.parametrize("warps", [1, 4])
 @pytest.mark.parametrize("cfg", sorted(ONE_TILE))
 @pytest.mark.parametrize("mistake", sorted(ONE_TILE_MISTAKES))
-def test_one_tile_planted_mistakes(cfg, mistake):
+def test_one_tile_planted_mistakes(cfg, mistake, warps):
     if cfg == "d192" and mistake == "no_s_buffer_wait":
         pytest.skip("d = 192 has no such wait (P has columns of its own)")
     caught = False
     for seed in range(400):
         try:
             run_one_tile(random_one_tile_units(random.Random(seed * 7 + 1)), seed,
-                         mistake=mistake, **ONE_TILE[cfg])
+                         mistake=mistake, warps=warps, **ONE_TILE[cfg])
         except Hazard:
             caught = True
             break
