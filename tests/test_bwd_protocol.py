@@ -19,8 +19,11 @@ Regions and the steps that may touch them:
 - Shared memory: K, V, the Q stages with their rows, dO and dS^T.
 
 Every MMA, load and compute step checks the contents it reads and that
-nothing it overwrites is still unread. The deterministic mode's cross-CTA
-semaphores are outside this model; the schedule tests cover their order.
+nothing it overwrites is still unread. The model runs each warpgroup as one
+actor, and also as four warps that arrive on their own, each owning a quarter
+of the key rows. In that mode every barrier phase must hold arrivals for a
+single step or unit. The deterministic mode's cross-CTA semaphores are
+outside this model; the schedule tests cover their order.
 """
 import random
 
@@ -29,24 +32,28 @@ import pytest
 from test_fwd_protocol import Hazard, Sim
 
 
-def run_bwd(units, seed, alias, mistake=None):
+def run_bwd(units, seed, alias, mistake=None, warps=1):
     """units: list of ni, the query tiles each key/value unit walks (0: a key
-    tile no query sees, as with unequal lengths)."""
-    sim = Sim([(n,) for n in units], seed, consumers=5)  # dO, MMA, 2 compute, drain
+    tile no query sees, as with unequal lengths).  warps: each compute
+    warpgroup and the drain as one actor (1), or as four warps arriving on
+    their own (4), each owning a quarter of the key rows."""
+    parts = 2 * warps  # compute actors: query-column half x key-row quarter
+    sim = Sim([(n,) for n in units], seed, consumers=3 + parts + warps - 1)
     for name in ("kv_full", "kv_empty", "do_full", "do_empty", "s_full", "dp_full", "s_free",
                  "ds_free", "dq_full", "dkv_full"):
         sim.bar(name)
     for name in ("p_ready", "ds_ready"):
-        sim.bar(name, 2)  # both compute warpgroups
+        sim.bar(name, parts)
     for name in ("dq_free", "dkv_free"):
-        sim.bar(name)
+        sim.bar(name, warps)
     for s in (0, 1):
         sim.bar(f"q_full{s}", 2)  # the TMA bytes' arrival + the rows' arrival
         sim.bar(f"q_empty{s}")
     smem = {}
-    st = {"rows": {}, "rows_read": {}, "S": [None, None], "P_read": True, "dP": None,
-          "dP_read": set([0, 1]), "dQ": None, "dQ_read": True, "dS": [None, None],
-          "dS_read": 2, "dK": [], "dV": [], "dkv_read": True, "do_read": True,
+    everyone, drainers = set(range(parts)), set(range(warps))
+    st = {"rows": {}, "rows_read": {}, "S": [None] * parts, "P_read": True, "dP": None,
+          "dP_read": set(everyone), "dQ": None, "dQ_read": set(drainers), "dS": [None] * parts,
+          "dS_read": 2, "dK": [], "dV": [], "dkv_read": set(drainers), "do_read": True,
           "kv_read": True, "q_read": {}}
 
     def producer():
@@ -71,7 +78,7 @@ def run_bwd(units, seed, alias, mistake=None):
                 if mistake != "no_q_empty_wait":
                     while not sim.ready(f"q_empty{q}", ((c >> 1) & 1) ^ 1, c >> 1):
                         yield
-                if st["q_read"].get(q) is False or st["rows_read"].get(q, 2) != 2:
+                if st["q_read"].get(q) is False or st["rows_read"].get(q, parts) != parts:
                     raise Hazard(f"Q stage {q} reloaded while still read")
                 st["q_read"][q], st["rows_read"][q] = False, 0
                 sim.load(f"q_full{q}", f"q{q}", (uid, s))
@@ -165,7 +172,7 @@ def run_bwd(units, seed, alias, mistake=None):
             it_unit += 1
             yield
 
-    def compute(h):
+    def compute(pt):
         it_sched = cnt = 0
         while True:
             unit = yield from sim.take(it_sched)
@@ -179,32 +186,34 @@ def run_bwd(units, seed, alias, mistake=None):
                     yield
                 while not sim.ready("s_full", cnt & 1, cnt + 1):
                     yield
-                if st["S"][h] != ("S", uid, s) or st["rows"].get(q) != (uid, s):
-                    raise Hazard(f"compute {h} ({uid},{s}) read {st['S'][h]}, rows {st['rows'].get(q)}")
+                if st["S"][pt] != ("S", uid, s) or st["rows"].get(q) != (uid, s):
+                    raise Hazard(f"compute {pt} ({uid},{s}) read {st['S'][pt]}, rows {st['rows'].get(q)}")
                 yield  # P^T = exp2(S^T - LSE)
-                st["S"][h] = ("P", uid, s)
-                sim.bars["p_ready"].arrive()
+                st["S"][pt] = ("P", uid, s)
+                sim.bars["p_ready"].arrive((uid, s))
                 while not sim.ready("dp_full", cnt & 1, cnt + 1):
                     yield
                 if cnt > 0 and mistake != "no_ds_free_wait":
                     while not sim.ready("ds_free", (cnt - 1) & 1, cnt):
                         yield
                 if st["dP"] != (uid, s) or st["rows"].get(q) != (uid, s):
-                    raise Hazard(f"compute {h} ({uid},{s}) read dP {st['dP']}")
-                if st["dS_read"] != 2:
+                    raise Hazard(f"compute {pt} ({uid},{s}) read dP {st['dP']}")
+                # this part's slice of the last complete dS^T tile must have been
+                # read by both dQ and dK before it is overwritten
+                if st["dS"][pt] is not None and st["dS_read"] != 2:
                     raise Hazard(f"dS of ({uid},{s}) written before dQ and dK read the last")
                 yield  # dS^T = P^T (dP^T - D)
                 if st["dP"] != (uid, s):
                     raise Hazard("dP overwritten while compute read it")
-                st["dP_read"].add(h)
+                st["dP_read"].add(pt)
                 st["rows_read"][q] = st["rows_read"].get(q, 0) + 1
-                st["dS"][h] = (uid, s)
-                if st["dS"] == [(uid, s), (uid, s)]:
+                st["dS"][pt] = (uid, s)
+                if st["dS"] == [(uid, s)] * parts:
                     st["dS_read"] = 0
-                sim.bars["ds_ready"].arrive()
+                sim.bars["ds_ready"].arrive((uid, s))
                 cnt += 1
 
-    def drain():
+    def drain(w):
         it_sched = it_unit = cnt = 0
         while True:
             unit = yield from sim.take(it_sched)
@@ -215,12 +224,12 @@ def run_bwd(units, seed, alias, mistake=None):
             for s in range(ni):
                 while not sim.ready("dq_full", cnt & 1, cnt + 1):
                     yield
-                for _ in range(2):  # reads the dQ row over a while
+                for _ in range(2):  # reads its dQ rows over a while
                     if st["dQ"] != (uid, s):
-                        raise Hazard(f"drain read dQ {st['dQ']}, expected {(uid, s)}")
+                        raise Hazard(f"drain warp {w} read dQ {st['dQ']}, expected {(uid, s)}")
                     yield
-                st["dQ_read"] = True
-                sim.bars["dq_free"].arrive()
+                st["dQ_read"].add(w)
+                sim.bars["dq_free"].arrive((uid, s))
                 cnt += 1
             while not sim.ready("dkv_full", it_unit & 1, it_unit + 1):
                 yield
@@ -229,9 +238,10 @@ def run_bwd(units, seed, alias, mistake=None):
                 if ni and (st["dK"] != want or st["dV"] != want):
                     raise Hazard(f"epilogue of {uid} read dK {st['dK']}, dV {st['dV']}")
                 yield
-            st["dkv_read"] = True
-            sim.out.append(("stored", uid))
-            sim.bars["dkv_free"].arrive()
+            st["dkv_read"].add(w)
+            if w == 0:
+                sim.out.append(("stored", uid))
+            sim.bars["dkv_free"].arrive(uid)
             it_unit += 1
 
     def execute(op, arg):
@@ -250,49 +260,51 @@ def run_bwd(units, seed, alias, mistake=None):
                 raise Hazard(f"S ({uid},{s}) read Q {smem.get(f'q{q}')}, K {smem.get('k')}")
             if not st["P_read"]:
                 raise Hazard(f"S ({uid},{s}) overwrote P^T {st['S']} before dV read it")
-            st["S"], st["P_read"] = [("S", uid, s)] * 2, False
+            st["S"], st["P_read"] = [("S", uid, s)] * parts, False
         elif op == "dP":
             uid, s = arg
             if smem.get("v") != uid or smem.get("do") != (uid, s):
                 raise Hazard(f"dP ({uid},{s}) read V {smem.get('v')}, dO {smem.get('do')}")
-            if st["dP_read"] != {0, 1}:
+            if st["dP_read"] != everyone:
                 raise Hazard(f"dP ({uid},{s}) overwrote dP {st['dP']} before compute read it")
-            if alias and not st["dQ_read"]:
+            if alias and st["dQ_read"] != drainers:
                 raise Hazard(f"dP ({uid},{s}) overwrote dQ {st['dQ']} before the drain read it")
             st["dP"], st["dP_read"] = (uid, s), set()
         elif op == "dV":
             uid, s = arg
-            if st["S"] != [("P", uid, s)] * 2 or smem.get("do") != (uid, s):
+            if st["S"] != [("P", uid, s)] * parts or smem.get("do") != (uid, s):
                 raise Hazard(f"dV ({uid},{s}) read {st['S']}, dO {smem.get('do')}")
             if s == 0:
-                if not st["dkv_read"]:
+                if st["dkv_read"] != drainers:
                     raise Hazard(f"dV of {uid} reset before the epilogue read the last")
                 st["dV"] = []
             st["dV"].append((uid, s))
             st["P_read"] = True
         elif op == "dQ":
             uid, s = arg
-            if st["dS"] != [(uid, s)] * 2 or smem.get("k") != uid:
+            if st["dS"] != [(uid, s)] * parts or smem.get("k") != uid:
                 raise Hazard(f"dQ ({uid},{s}) read dS {st['dS']}")
-            if not st["dQ_read"]:
+            if st["dQ_read"] != drainers:
                 raise Hazard(f"dQ ({uid},{s}) overwrote dQ {st['dQ']} before the drain read it")
-            if alias and st["dP_read"] != {0, 1}:
+            if alias and st["dP_read"] != everyone:
                 raise Hazard(f"dQ ({uid},{s}) overwrote dP before compute read it")
-            st["dQ"], st["dQ_read"] = (uid, s), False
+            st["dQ"], st["dQ_read"] = (uid, s), set()
             if alias:
                 st["dP"] = None  # its columns now hold dQ
             st["dS_read"] += 1
         elif op == "dK":
             uid, s, q = arg
-            if st["dS"] != [(uid, s)] * 2 or smem.get(f"q{q}") != (uid, s):
+            if st["dS"] != [(uid, s)] * parts or smem.get(f"q{q}") != (uid, s):
                 raise Hazard(f"dK ({uid},{s}) read dS {st['dS']}, Q {smem.get(f'q{q}')}")
             if s == 0:
                 st["dK"] = []
-                st["dkv_read"] = False  # both accumulators now hold this unit's
+                st["dkv_read"] = set()  # both accumulators now hold this unit's
             st["dK"].append((uid, s))
             st["dS_read"] += 1
 
-    sim.run([producer(), do_producer(), mma(), compute(0), compute(1), drain()], execute, smem)
+    roles = [producer(), do_producer(), mma()] + [compute(pt) for pt in range(parts)] + [
+        drain(w) for w in range(warps)]
+    sim.run(roles, execute, smem)
     if sorted(sim.out) != [("stored", u) for u in range(len(units))]:
         raise Hazard(f"outputs {sim.out}")
 
@@ -303,10 +315,11 @@ def random_units(rnd):
     return [rnd.choice([0, 1, 1, 2, 3, 5, 8]) for _ in range(rnd.randint(0, 6))]
 
 
+@pytest.mark.parametrize("warps", [1, 4])
 @pytest.mark.parametrize("alias", [True, False], ids=["d128", "d64"])
-def test_bwd_protocol_is_hazard_and_deadlock_free(alias):
-    for seed in range(300):
-        run_bwd(random_units(random.Random(seed * 11 + 5)), seed, alias)
+def test_bwd_protocol_is_hazard_and_deadlock_free(alias, warps):
+    for seed in range(300 if warps == 1 else 150):
+        run_bwd(random_units(random.Random(seed * 11 + 5)), seed, alias, warps=warps)
 
 
 # Mistakes the model must catch (True), and waits it shows to be implied by
@@ -323,12 +336,13 @@ BWD_MISTAKES = {"no_q_empty_wait": True, "no_do_empty_wait": True, "no_dq_free_w
                 "no_empty_unit_dkv_wait": True}
 
 
+@pytest.mark.parametrize("warps", [1, 4])
 @pytest.mark.parametrize("mistake", sorted(BWD_MISTAKES))
-def test_bwd_planted_mistakes(mistake):
+def test_bwd_planted_mistakes(mistake, warps):
     caught = False
     for seed in range(300):
         try:
-            run_bwd(random_units(random.Random(seed * 11 + 5)), seed, True, mistake)
+            run_bwd(random_units(random.Random(seed * 11 + 5)), seed, True, mistake, warps)
         except Hazard:
             caught = True
             break
