@@ -28,8 +28,8 @@ Layouts modelled:
 - d = 192: as d = 256 but with whole V tiles over 2 slots and P in TMEM
   columns of its own.
 
-The one-tile model also runs its softmax and epilogue warpgroups as four
-warps each, each arriving on its own and owning a quarter of the rows. Each
+Both models also run their softmax (and epilogue) warpgroups as four warps
+each, each arriving on its own and owning a quarter of the rows. Each
 arrival carries the step or unit it stands for, and a phase that completes
 with arrivals for two different ones is a hazard: a fast warp must never
 arrive for its next step inside the phase its neighbours are completing.
@@ -158,13 +158,17 @@ def check_outputs(sim, keyless):
 
 # ------------------------------------------------------------------ d <= 128
 
-def run_two_tile(units, seed, stages, mistake=None):
+def run_two_tile(units, seed, stages, mistake=None, warps=1):
     """units: list of (n0, n1, nkv): key/value steps of query tiles 0 and 1 (0:
-    past the end, or no row sees a key), and tiles loaded (>= 1)."""
-    sim = Sim(units, seed, consumers=3)  # MMA issuer + two softmax warpgroups
+    past the end, or no row sees a key), and tiles loaded (>= 1).  warps: each
+    tile's softmax warpgroup as one actor (1), or as four warps arriving on
+    their own (4), each owning a quarter of the rows."""
+    sim = Sim(units, seed, consumers=1 + 2 * warps)  # MMA issuer + the softmax warps
     for t in (0, 1):
-        for name in ("s_full", "p_full", "o_done", "o_free"):
+        for name in ("s_full", "o_done"):
             sim.bar(f"{name}{t}")
+        for name in ("p_full", "o_free"):
+            sim.bar(f"{name}{t}", warps)
     for name in ("q_full", "q_empty"):
         sim.bar(name)
     for s in range(stages):
@@ -253,7 +257,7 @@ def run_two_tile(units, seed, stages, mistake=None):
             for t in (0, 1):
                 ep[t] += n[t] > 0
 
-    def softmax(t):
+    def softmax(t, w):
         it_sched = it = 0
         while True:
             unit = yield from sim.take(it_sched)
@@ -268,14 +272,14 @@ def run_two_tile(units, seed, stages, mistake=None):
                 while not sim.ready(f"s_full{t}", it & 1, it + 1):
                     yield
                 if st["S"].get(t) != (uid, j):
-                    raise Hazard(f"softmax {t} ({uid},{j}) read S = {st['S'].get(t)}")
+                    raise Hazard(f"softmax {t}.{w} ({uid},{j}) read S = {st['S'].get(t)}")
                 yield  # the exponentials
                 if st["S"].get(t) != (uid, j):
                     raise Hazard("S overwritten while the softmax read it")
-                st["P"][t] = (uid, j)
+                st["P"].setdefault(t, {})[w] = (uid, j)
                 if j > 0 and sim.rnd.random() < 0.3 and st["O"][t] != [(uid, q) for q in range(j)]:
                     raise Hazard(f"rescale of tile {t} ({uid},{j}) saw O = {st['O'][t]}")
-                sim.bars[f"p_full{t}"].arrive()
+                sim.bars[f"p_full{t}"].arrive((uid, j))
                 it += 1
                 yield
             while not sim.ready(f"o_done{t}", (it - 1) & 1, it):
@@ -284,8 +288,9 @@ def run_two_tile(units, seed, stages, mistake=None):
                 if st["O"][t] != [(uid, q) for q in range(nt)]:
                     raise Hazard(f"epilogue of tile {t} of {uid} read O = {st['O'][t]}")
                 yield
-            sim.out.append(("stored", (uid, t)))
-            sim.bars[f"o_free{t}"].arrive()
+            if w == 0:
+                sim.out.append(("stored", (uid, t)))
+            sim.bars[f"o_free{t}"].arrive(uid)
 
     def execute(op, arg):
         if op == "commit":
@@ -298,19 +303,22 @@ def run_two_tile(units, seed, stages, mistake=None):
             uid, t, j, s = arg
             if smem.get(f"q{t}") != uid or smem.get(f"k{s}") != (uid, j):
                 raise Hazard(f"S_{t} ({uid},{j}) read Q {smem.get(f'q{t}')}, K {smem.get(f'k{s}')}")
-            if st["P"].get(t) not in (None, "read"):
+            if any(v != "read" for v in st["P"].get(t, {}).values()):
                 raise Hazard(f"S_{t} ({uid},{j}) overwrote P {st['P'][t]} before PV read it")
-            st["S"][t], st["P"][t] = (uid, j), None
+            st["S"][t], st["P"][t] = (uid, j), {}
         elif op == "PV":
             uid, t, j, s = arg
-            if smem.get(f"v{s}") != (uid, j) or st["P"].get(t) != (uid, j):
-                raise Hazard(f"PV_{t} ({uid},{j}) read V {smem.get(f'v{s}')}, P {st['P'].get(t)}")
+            quarters = st["P"].get(t, {})
+            if smem.get(f"v{s}") != (uid, j) or len(quarters) != warps or any(
+                    v != (uid, j) for v in quarters.values()):
+                raise Hazard(f"PV_{t} ({uid},{j}) read V {smem.get(f'v{s}')}, P {quarters}")
             if j == 0:
                 st["O"][t] = []
             st["O"][t].append((uid, j))
-            st["P"][t] = "read"
+            st["P"][t] = {q: "read" for q in quarters}
 
-    sim.run([producer(), mma(), softmax(0), softmax(1)], execute, smem)
+    roles = [producer(), mma()] + [softmax(t, w) for t in (0, 1) for w in range(warps)]
+    sim.run(roles, execute, smem)
     check_outputs(sim, [((u, t), units[u][t] == 0) for u in range(len(units)) for t in (0, 1)
                         if units[u][t] > 0])
 
@@ -337,10 +345,12 @@ def random_two_tile_units(rnd):
     return units
 
 
+@pytest.mark.parametrize("warps", [1, 4])
 @pytest.mark.parametrize("stages", [2, 4])
-def test_two_tile_protocol_is_hazard_and_deadlock_free(stages):
-    for seed in range(300):
-        run_two_tile(random_two_tile_units(random.Random(seed * 7 + 3)), seed, stages)
+def test_two_tile_protocol_is_hazard_and_deadlock_free(stages, warps):
+    for seed in range(300 if warps == 1 else 150):
+        run_two_tile(random_two_tile_units(random.Random(seed * 7 + 3)), seed, stages,
+                     warps=warps)
 
 
 # Mistakes the model must catch (True), and waits it shows to be implied by
@@ -353,12 +363,14 @@ TWO_TILE_MISTAKES = {"no_s_wait": False, "no_o_free_wait": False, "no_kv_empty_w
                      "no_q_empty_wait": True}
 
 
+@pytest.mark.parametrize("warps", [1, 4])
 @pytest.mark.parametrize("mistake", sorted(TWO_TILE_MISTAKES))
-def test_two_tile_planted_mistakes(mistake):
+def test_two_tile_planted_mistakes(mistake, warps):
     caught = False
     for seed in range(300):
         try:
-            run_two_tile(random_two_tile_units(random.Random(seed * 7 + 3)), seed, 2, mistake)
+            run_two_tile(random_two_tile_units(random.Random(seed * 7 + 3)), seed, 2, mistake,
+                         warps)
         except Hazard:
             caught = True
             break
