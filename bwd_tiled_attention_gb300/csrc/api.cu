@@ -127,6 +127,13 @@ fa_status check_shape(int B, int Hq, int Hkv, int Nq, int total_q, int Nk, int t
 
 fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// A packed batch is ranked by one scheduler CTA, with a prefix entry per tile
+// level of the longest sequence: its bound N must fit one CTA's shared memory.
+constexpr size_t kSchedSmemMax = 232448;  // 227 KB, the per-block maximum
+bool sched_fits(const Shape& s, int N, int rows) {
+    return !s.varlen || sched_smem_bytes(s.B, cdiv(N, rows)) <= kSchedSmemMax;
+}
+
 // Queries and keys provably have equal lengths (the same boundary array, or a
 // dense batch with Nq = Nk): the kernels' square instantiation applies.
 bool same_boundaries(const Shape& s, const int* cu_q, const int* cu_k) {
@@ -145,6 +152,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, fa_dtyp
     if (o_dtype != FA_BF16 && o_dtype != FA_FP32) return FA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_UNSUPPORTED;
     if (s.Tq == 0 || B == 0) return FA_OK;  // nothing to compute
+    if (!sched_fits(s, Nq, d > 128 ? kFwdBlockRowsWide : kFwdBlockRows)) return FA_ERR_UNSUPPORTED;
     if (!q || !o || !lse || !workspace || (s.Tk > 0 && (!k || !v))) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
         !aligned16(workspace))
@@ -204,6 +212,7 @@ fa_status bwd_preprocess_impl(const void* o, fa_dtype o_dtype, const void* dout,
     if (d > 128) return FA_ERR_UNSUPPORTED;  // the backward keeps 256 + 2d TMEM columns
     if (o_dtype != FA_BF16 && o_dtype != FA_FP32) return FA_ERR_INVALID_ARG;
     if (s.Tq == 0 || s.Tk == 0 || B == 0) return FA_OK;  // fa_bwd needs no workspace then
+    if (!sched_fits(s, Nk, kTile)) return FA_ERR_UNSUPPORTED;  // units are key/value tiles
     if (!o || !dout || !D || !workspace) return FA_ERR_INVALID_ARG;
     if (!aligned16(o) || !aligned16(dout) || !aligned4(D) || !aligned16(workspace))
         return FA_ERR_INVALID_ARG;
@@ -251,6 +260,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* dout
         if (e == cudaSuccess && out1) e = cudaMemsetAsync(out1, 0, n * elem_bytes(grad_dtype), strm);
         return cuda_status(e);
     }
+    if (!sched_fits(s, Nk, kTile)) return FA_ERR_UNSUPPORTED;  // as fa_bwd_preprocess
     if (!q || !k || !v || !dout || !lse || !D || !dq || !dk || !dv || !workspace)
         return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) ||

@@ -57,6 +57,10 @@ cudaError_t launch_sched(const int* cu_seqlens, int B, int N, int T, int H, int 
                          size_t tile_off_off, bool want_tile_off, const int* cu_tiles_seqlens,
                          int N_tiles, int T_tiles, cudaStream_t stream);
 
+// Dynamic shared memory the scheduler needs for a packed batch of B sequences
+// whose longest spans at most maxnt_bound tiles (one CTA ranks them all).
+size_t sched_smem_bytes(int B, int maxnt_bound);
+
 cudaError_t launch_fwd(const FwdParams& p, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, float* D,

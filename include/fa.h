@@ -44,6 +44,15 @@
  *   when j > i (positions within the sequence; queries and keys have equal
  *   length).  The *_kv calls take separate query and key/value lengths; their
  *   causal mask is described at fa_fwd_kv.
+ * - Size limits (FA_ERR_UNSUPPORTED, nothing launched): Hq <= 65535; every
+ *   sequence bound N (Nq, Nk) within 65535 tiles of 128 tokens; a dense
+ *   batch's B*N < 2^31; T * Hq * d <= 2^40 on either side.  A packed batch
+ *   has B <= 4096 sequences.  One scheduler CTA ranks a packed batch, keeping
+ *   8 bytes per tile level of the longest sequence in its shared memory, so
+ *   there N must also satisfy 16 * ceil(3B / 4) + 8 * (max(B, ceil(N / R)) + 1)
+ *   <= 227 KB. R is the work unit's height: 256 rows for the forward up to
+ *   d = 128, 128 rows otherwise, and the backward's key/value units.  That
+ *   is N <= ~3.7M tokens, or ~7.4M for the forward up to d = 128.
  * - Every call is asynchronous on `stream` (NULL = the legacy default stream)
  *   and never synchronises, except fa_check_device_status.  The return value
  *   reports argument validation and launch errors only; it never aborts.

@@ -120,6 +120,28 @@ def test_bwd_rejects_bad_arguments(L):
     assert fa.fa_bwd_preprocess(**dict(pre, o_dtype=9)) == fa.FA_ERR_INVALID_ARG
 
 
+def test_packed_sequence_bound_fits_the_scheduler(L):
+    """A packed batch is ranked by one scheduler CTA with 8 bytes per tile level
+    of its longest sequence: past 227 KB of shared memory the calls refuse,
+    before launching anything, what they would otherwise fail to launch.  The
+    level height is the work unit's: 256 rows for the forward up to d = 128,
+    128 otherwise.  Inside the bound the arguments pass validation (on a
+    machine without a GPU the first CUDA call then fails)."""
+    packed = dict(cu_seqlens=FAKE, total_tokens=10)
+    assert fwd_call(d=256, N=4_000_000, **packed) == fa.FA_ERR_UNSUPPORTED
+    assert fwd_call(d=64, N=8_000_000, **packed) == fa.FA_ERR_UNSUPPORTED
+    assert fwd_call(d=64, N=4_000_000, **packed) != fa.FA_ERR_UNSUPPORTED   # 256-row units
+    assert fwd_call(d=256, N=3_600_000, **packed) != fa.FA_ERR_UNSUPPORTED
+    assert bwd_call(N=4_000_000, **packed) == fa.FA_ERR_UNSUPPORTED
+    assert bwd_call(N=3_600_000, **packed) != fa.FA_ERR_UNSUPPORTED
+    pre = dict(o=FAKE, o_dtype=fa.FA_BF16, dout=FAKE, D=FAKE, workspace=FAKE,
+               workspace_bytes=1 << 30, B=2, Hq=4, Hkv=2, N=4_000_000, total_tokens=10, d=128,
+               causal=1, cu_seqlens=FAKE, deterministic=0, stream=0)
+    assert fa.fa_bwd_preprocess(**pre) == fa.FA_ERR_UNSUPPORTED
+    # dense batches have no such bound (their order is closed-form)
+    assert fwd_call(d=256, B=1, N=4_000_000) != fa.FA_ERR_UNSUPPORTED
+
+
 def fwd_kv_call(**kw):
     args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, o_dtype=fa.FA_BF16, lse=FAKE, B=2, Hq=4, Hkv=2,
                 Nq=64, total_q=0, Nk=200, total_k=0, d=128, scale=0.125, causal=1,
