@@ -30,7 +30,7 @@ from . import build as _build
 __all__ = [
     "FAError", "lib", "fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_fwd_workspace_size",
     "fa_bwd_workspace_size", "fa_bwd_workspace_semaphore_offset", "fa_check_device_status",
-    "fa_bwd_noalloc", "fa_fwd_kv", "fa_bwd_kv_workspace_size", "fa_bwd_kv_preprocess", "fa_bwd_kv",
+    "fa_bwd_noalloc", "fa_noalloc_check_device_status", "fa_fwd_kv", "fa_bwd_kv_workspace_size", "fa_bwd_kv_preprocess", "fa_bwd_kv",
     "fa_status_string", "forward", "backward", "attention", "FA_OK", "FA_ERR_INVALID_ARG",
     "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_BF16", "FA_FP32",
 ]
@@ -59,6 +59,7 @@ _SIGS = {
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _i, _i, _i, _i, _i,
                     _i, _f, _i, _vp, _i, _vp]),
     "fa_check_device_status": (_i, [_vp, _vp]),
+    "fa_noalloc_check_device_status": (_i, [_vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                             _i, _i, _f, _i, _vp, _i, _vp]),
     "fa_fwd_kv": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp,
@@ -215,6 +216,11 @@ def fa_bwd_kv(q, k, v, dout, lse, D, dq, dk, dv, grad_dtype, workspace, workspac
 
 def fa_check_device_status(workspace, stream=None) -> int:
     return int(lib().fa_check_device_status(_ptr(workspace), _stream(stream)))
+
+
+def fa_noalloc_check_device_status(stream=None) -> int:
+    """Device status of the last fa_bwd_noalloc call on the current device (synchronises)."""
+    return int(lib().fa_noalloc_check_device_status(_stream(stream)))
 
 
 # ----------------------------------------------------------------------------- tensor API

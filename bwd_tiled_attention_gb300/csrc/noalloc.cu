@@ -14,7 +14,14 @@
 // library is loaded holds kNoAllocScratchBytes for it until the process exits.
 // Host code cannot use the array's name as a device address, so the first call
 // on each device looks the address up with cudaGetSymbolAddress (with that
-// device current) and caches it.
+// device current) and caches it.  cudaDeviceReset destroys the context that
+// address belongs to; the cache is not told, so no call may follow a reset.
+//
+// Layout of the array: the backward workspace first, so its header -- and the
+// device error word at its offset 0 -- sits at the array's base on every
+// call, then D.  fa_noalloc_check_device_status reads that word, which is how
+// a caller of fa_bwd_noalloc learns of errors found inside the kernels (a
+// bounded wait that gave up, a sequence longer than N).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -66,8 +73,8 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
     void* scratch = nullptr;
     fa_status st = scratch_on_current_device(&scratch);
     if (st != FA_OK) return st;
-    float* D = static_cast<float*>(scratch);
-    void* ws = static_cast<char*>(scratch) + d_bytes;
+    void* ws = scratch;  // error word at the array's base
+    float* D = reinterpret_cast<float*>(static_cast<char*>(scratch) + ws_bytes);
     // fa_bwd_preprocess clears everything in the workspace that must start at
     // zero (dQ accumulator, semaphores, work counter, error word).
     st = fa_bwd_preprocess(o, o_dtype, dout, D, ws, ws_bytes, B, Hq, Hkv, N, total_tokens, d,
@@ -75,4 +82,11 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
     if (st != FA_OK) return st;
     return fa_bwd(q, k, v, dout, lse, D, dq, dk, dv, grad_dtype, ws, ws_bytes, B, Hq, Hkv, N,
                   total_tokens, d, scale, causal, cu_seqlens, deterministic, stream);
+}
+
+extern "C" fa_status fa_noalloc_check_device_status(fa_stream_t stream) {
+    void* scratch = nullptr;
+    const fa_status st = scratch_on_current_device(&scratch);
+    if (st != FA_OK) return st;
+    return fa_check_device_status(scratch, stream);
 }

@@ -245,12 +245,26 @@ fa_status fa_bwd_kv(const void* q, const void* k, const void* v, const void* dou
  *   parts that must start at zero are cleared on every call): calls that can
  *   overlap on the GPU -- on different streams, or from different host
  *   threads -- race on it and must be serialised by the caller.
+ *   Errors found inside the kernels (a bounded wait that gave up, a sequence
+ *   longer than N) are recorded in the array, not returned: read them with
+ *   fa_noalloc_check_device_status after the call.  The cached array address
+ *   belongs to the device's context: after cudaDeviceReset no call may be made.
  */
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                          fa_dtype o_dtype, const void* dout, const float* lse, void* dq, void* dk,
                          void* dv, fa_dtype grad_dtype, int B, int Hq, int Hkv, int N,
                          int total_tokens, int d, float scale, int causal, const int* cu_seqlens,
                          int deterministic, fa_stream_t stream);
+
+/*
+ * Device status of the last fa_bwd_noalloc call on the current device: as
+ * fa_check_device_status, on the error word that the call's kernels keep at
+ * the base of the library's scratch array.  Synchronises `stream` (pass the
+ * stream of that call).  FA_OK if no fa_bwd_noalloc call has run on the device.
+ * The pages have no counterpart of this call: it completes fa_bwd_noalloc,
+ * whose caller holds no workspace to pass to fa_check_device_status.
+ */
+fa_status fa_noalloc_check_device_status(fa_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads the device error word of a backward or

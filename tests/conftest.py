@@ -25,3 +25,22 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With FA_PARITY_REPORT set, write every recorded comparison (test,
+    tensor, relative Frobenius error, un-discounted max-abs, max |ref|) there
+    as JSON."""
+    path = os.environ.get("FA_PARITY_REPORT")
+    if not path:
+        return
+    try:
+        import json
+
+        from harness import RECORDS
+    except Exception:  # pragma: no cover
+        return
+    d = os.path.dirname(os.path.abspath(path))
+    os.makedirs(d, exist_ok=True)
+    with open(path, "w") as f:
+        json.dump(RECORDS, f, indent=0)

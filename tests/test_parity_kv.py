@@ -48,14 +48,15 @@ def kv_inputs(lq, lk, Hq, Hkv, d, seed):
     return inp, x
 
 
-def run_kv(x, lq, lk, causal, scale, deterministic=False, grad_dtype=torch.bfloat16):
-    """Forward + backward; O is stored in the gradients' dtype, so the fp32
-    pass has no bf16 storage rounding anywhere at the API boundary (a bf16 O
-    feeds its rounding into D = rowsum(dO * O) and from there into dK)."""
+def run_kv(x, lq, lk, causal, scale, deterministic=False, grad_dtype=torch.bfloat16,
+           out_dtype=None):
+    """Forward + backward; O is stored in out_dtype, by default the gradients'
+    dtype (a bf16 O feeds its rounding into D = rowsum(dO * O) and from there
+    into dK)."""
     kw = dict(cu_seqlens=x["cu_seqlens"], max_seqlen=max(max(lq), 1),
               cu_seqlens_k=x["cu_seqlens_k"], max_seqlen_k=max(max(lk), 1))
-    o, lse = fa.forward(x["q"], x["k"], x["v"], causal=causal, scale=scale, out_dtype=grad_dtype,
-                        **kw)
+    o, lse = fa.forward(x["q"], x["k"], x["v"], causal=causal, scale=scale,
+                        out_dtype=grad_dtype if out_dtype is None else out_dtype, **kw)
     dq, dk, dv = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=causal,
                              scale=scale, deterministic=deterministic, grad_dtype=grad_dtype,
                              check_status=True, **kw)
@@ -77,9 +78,45 @@ def test_kv_parity(name, lq, lk, Hq, Hkv, d, causal, deterministic):
     assert_lse_kv(to_np(got["lse"]), ref["lse"])
     for g in ("dq", "dk", "dv"):
         assert_close(g, to_np(got[g]), ref[g])
-    g32 = run_kv(x, lq, lk, causal, scale, deterministic, grad_dtype=torch.float32)
-    for g in ("dq", "dk", "dv"):
-        assert_close(g + " (fp32 out)", to_np(g32[g]), ref[g], stored_bf16=False)
+    # the literal bound on fp32 gradients, with the default bf16 O and with O in fp32
+    for o_dt in (torch.bfloat16, torch.float32):
+        g32 = run_kv(x, lq, lk, causal, scale, deterministic, grad_dtype=torch.float32,
+                     out_dtype=o_dt)
+        for g in ("dq", "dk", "dv"):
+            got32 = to_np(g32[g])
+            label = f"{g} (fp32 out, {str(o_dt)[6:]} O)"
+            if (name, causal, g, o_dt) == ("d64_mqa", True, "dk", torch.bfloat16):
+                keys_beyond_bound(inp, oi, ref, got32, scale, label)
+            else:
+                assert_close(label, got32, ref[g], stored_bf16=False)
+
+
+def keys_beyond_bound(inp, oi, ref, dk, scale, label):
+    """The one output of these cases that passes the absolute bound of 2e-2:
+    dK of key 0 of sequence 1 (100 queries and 100 keys, 6 query heads on one
+    key/value head, d = 64) with the default bf16 O, off by 0.0216 at a
+    relative Frobenius error of 2.4e-3.  The rounding model
+    (tests/rounding_model.py: the kernels' bf16 rounding points in float64
+    numpy) lands exactly as far from the oracle there -- and 0.0184 with O in
+    fp32, under the bound, as the kernel does -- so the excess is the bf16
+    precision of P, dS and the stored O, not a defect.  Checked here: the
+    relative bound on the whole tensor, the literal bound on every other
+    sequence's keys, and the kernel within 3e-3 of the model on sequence 1."""
+    from rounding_model import grads
+    assert_close(label + " (relative)", dk, ref["dk"], stored_bf16=False, mabs=1.0)
+    cq, ck = inp["cu_seqlens"].numpy(), inp["cu_seqlens_k"].numpy()
+    b = 1
+    q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+    assert q1 - q0 == k1 - k0, "the model covers equal query and key lengths"
+    others = np.r_[0:k0, k1:dk.shape[0]]
+    assert_close(label + " other sequences", dk[others], ref["dk"][others], stored_bf16=False)
+    model = grads(oi["q"][q0:q1], oi["k"][k0:k1, 0], oi["v"][k0:k1, 0], oi["dout"][q0:q1],
+                  scale, True)
+    err_kernel = float(np.max(np.abs(dk[k0:k1] - ref["dk"][k0:k1])))
+    err_model = float(np.max(np.abs(model["dk"] - ref["dk"][k0:k1, 0])))
+    assert err_model > 2e-2 and err_kernel <= err_model + 3e-3, (err_kernel, err_model)
+    assert_close(label + " vs the rounding model", dk[k0:k1, 0], model["dk"], stored_bf16=False,
+                 mabs=3e-3)
 
 
 @pytest.mark.parametrize("causal", [False, True])
