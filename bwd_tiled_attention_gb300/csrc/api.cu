@@ -226,8 +226,9 @@ fa_status bwd_preprocess_impl(const void* o, fa_dtype o_dtype, const void* dout,
     const int order = deterministic ? kOrderLevelDesc : (causal ? kOrderWorkDesc : kOrderSeqDesc);
     char* ws = static_cast<char*>(workspace);
     // units are key/value tiles; dQ semaphores are numbered by query tile
-    cudaError_t e = launch_sched(cu_k, B, Nk, s.Tk, Hq, kTile, order, lay.max_units, workspace,
-                                 lay.units, lay.tile_off, true, cu_q, Nq, s.Tq, strm);
+    // units: (key/value tile, run of query heads), runs innermost
+    cudaError_t e = launch_sched(cu_k, B, Nk, s.Tk, Hkv * lay.nruns, kTile, order, lay.max_units,
+                                 workspace, lay.units, lay.tile_off, true, cu_q, Nq, s.Tq, strm);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     e = launch_bwd_preprocess(o, o_dtype == FA_FP32, dout, D,
                               reinterpret_cast<float*>(ws + lay.dq_acc),
@@ -295,16 +296,19 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* dout
     p.causal = causal ? 1 : 0;
     p.deterministic = deterministic ? 1 : 0;
     p.grad_fp32 = grad_dtype == FA_FP32;
+    p.hchunk = lay.hchunk;
+    p.nchunks = lay.nruns;
     const int nsm = sm_count();
     if (nsm <= 0) return FA_ERR_CUDA;
     cudaError_t e = launch_bwd(p, nsm, strm);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     char* ws = static_cast<char*>(workspace);
-    const bool gqa = Hq != Hkv;
+    const bool partials = lay.nruns > 1;
     e = launch_bwd_postprocess(reinterpret_cast<const float*>(ws + lay.dq_acc), dq,
-                               gqa ? reinterpret_cast<const float*>(ws + lay.dk_acc) : nullptr,
-                               gqa ? reinterpret_cast<const float*>(ws + lay.dv_acc) : nullptr,
-                               dk, dv, s.Tq, s.Tk, Hq, Hkv, d, scale, p.grad_fp32, nsm, strm);
+                               partials ? reinterpret_cast<const float*>(ws + lay.dk_acc) : nullptr,
+                               partials ? reinterpret_cast<const float*>(ws + lay.dv_acc) : nullptr,
+                               dk, dv, s.Tq, s.Tk, Hq, Hkv, lay.nruns, d, scale, p.grad_fp32, nsm,
+                               strm);
     return cuda_status(e);
 }
 

@@ -6,11 +6,17 @@
 // section 1.1): S = QK^T recomputed, P = exp(S - LSE) from the stored
 // logsumexp, dV += P^T dO, dP = dO V^T, dS = P * (dP - D), dK += dS^T Q,
 // dQ += dS K.  Work is parallel over key/value tiles ("FlashAttention-2-
-// ICLR24" 核心方法 2): a unit owns one key/value tile of one (sequence, query
-// head), keeps K_j, V_j and the dK_j, dV_j accumulators on chip, and walks the
-// query tiles; dQ is a sum over key/value tiles and is merged in global
-// memory, either with fp32 atomics or -- deterministic mode, section 3.2 of
-// the same page -- in a fixed order enforced by one semaphore per dQ tile.
+// ICLR24" 核心方法 2): a unit owns one key/value tile of one sequence and a
+// run of C query heads that share its key/value head, keeps K_j, V_j and the
+// dK_j, dV_j accumulators on chip, and walks the query tiles of each of its
+// heads in turn, accumulating dK_j and dV_j over all of them ("FlashAttention-
+// 4反向传播优化" section 5.2: for MQA/GQA, walk the query heads of a key/value
+// head before moving on).  C = 1 for MHA; with C equal to the group the unit
+// writes the final dK, dV, otherwise fp32 partials per run of heads that the
+// conversion kernel sums in a fixed order.  dQ is a sum over key/value tiles
+// and is merged in global memory, either with fp32 atomics or -- deterministic
+// mode, section 3.2 of the first page -- in a fixed order enforced by one
+// semaphore per dQ tile.
 //
 // Walk order (section 3.3.1): in deterministic mode the scheduler launches
 // units with descending j and every dQ tile takes its contributions in
@@ -96,24 +102,32 @@ struct BwdSmem {
 };
 static_assert(sizeof(BwdSmem<128>) <= 232448, "backward shared memory exceeds 227 KB");
 
-// One work unit: key/value tile j of sequence b, query head h (key/value head
-// g).  t0/L are the query tokens, tk0/Lk the key/value tokens; under the
-// causal mask query row r sees key c iff c <= r + off, off = Lk - L.  nt =
-// query tiles, ntk = key/value tiles, i0 = first query tile with a row that
-// sees a key of tile j, ni = query tiles the unit visits.
+// One work unit: key/value tile j of sequence b, key/value head g, query heads
+// h0 .. h0 + C - 1 (run uh of the runs of heads: the unit-list head field).
+// t0/L are the query tokens, tk0/Lk the key/value tokens; under the causal
+// mask query row r sees key c iff c <= r + off, off = Lk - L.  nt = query
+// tiles, ntk = key/value tiles, i0 = first query tile with a row that sees a
+// key of tile j, ni = query tiles the unit visits per head, ns = C * ni steps.
 struct BUnit {
-    int b, j, h, g, t0, L, tk0, Lk, off, nt, ntk, i0, ni;
+    int b, j, uh, g, h0, t0, L, tk0, Lk, off, nt, ntk, i0, ni, ns;
 };
 
 // KV = false: keys and queries share their boundaries (Lk = L, off = 0), and
-// the geometry is the plain square one.
-template <bool KV>
+// the geometry is the plain square one.  RUNS = false: one query head per
+// unit (the unit-list head field is that head); true: runs of p.hchunk > 1.
+template <bool KV, bool RUNS>
 __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
     BUnit x;
     x.b = u.x;
     x.j = unit_tile(u.y);
-    x.h = unit_head(u.y);
-    x.g = (int)(((long long)x.h * p.Hkv) / p.Hq);
+    x.uh = unit_head(u.y);
+    if constexpr (RUNS) {
+        x.g = x.uh / p.nchunks;
+        x.h0 = x.g * (p.Hq / p.Hkv) + (x.uh - x.g * p.nchunks) * p.hchunk;
+    } else {
+        x.h0 = x.uh;
+        x.g = (int)(((long long)x.uh * p.Hkv) / p.Hq);
+    }
     seq_bounds(p.cu_seqlens, p.N, x.b, x.t0, x.L);
     x.nt = cdiv(x.L, kTile);
     if constexpr (KV) {
@@ -130,6 +144,7 @@ __device__ __forceinline__ BUnit decode_bunit(int2 u, const BwdParams& p) {
         x.i0 = p.causal ? x.j : 0;
         x.ni = p.causal ? x.nt - x.j : x.nt;
     }
+    x.ns = RUNS ? x.ni * p.hchunk : x.ni;
     return x;
 }
 
@@ -145,6 +160,32 @@ template <bool KV>
 __device__ __forceinline__ int walk_tile(const BUnit& x, int s, int deterministic, int causal) {
     if (!causal) return s;
     return deterministic ? (KV ? x.i0 : x.j) + s : x.nt - 1 - s;
+}
+
+// Position in a unit's walk: the unit walks the query tiles of head h0, then
+// those of h0 + 1, ...; si = step within the current head, hh = head offset.
+struct StepPos {
+    int hh = 0, si = 0;
+    __device__ __forceinline__ void next(int ni) {
+        if (++si == ni) {
+            si = 0;
+            ++hh;
+        }
+    }
+};
+
+// Query head h and query tile i of step s of unit x (w: the walk position of
+// step s, used when the unit walks a run of heads).
+template <bool KV, bool RUNS>
+__device__ __forceinline__ void unit_step(const BUnit& x, int s, const StepPos& w,
+                                          const BwdParams& p, int& h, int& i) {
+    if constexpr (RUNS) {
+        h = x.h0 + w.hh;
+        i = walk_tile<KV>(x, w.si, p.deterministic, p.causal);
+    } else {
+        h = x.h0;
+        i = walk_tile<KV>(x, s, p.deterministic, p.causal);
+    }
 }
 
 // Deterministic mode: how many contributions to dQ tile i precede unit x's.
@@ -247,7 +288,7 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* l
 // DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros,
 // which add nothing to S or dP and make the last 32 columns of dV, dK and dQ
 // zero; those columns are neither stored nor merged.
-template <int D, int DR, bool KV>
+template <int D, int DR, bool KV, bool RUNS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
     pdl_trigger();
@@ -341,7 +382,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             unit.y = __shfl_sync(0xffffffffu, unit.y, 0);
             ++sched_it;
             if (unit.x < 0) break;
-            const BUnit x = decode_bunit<KV>(unit, p);
+            const BUnit x = decode_bunit<KV, RUNS>(unit, p);
             if (!(ok = lane0_wait(smem_u32(&sm.kv_empty), (unit_it & 1) ^ 1, abort_flag, hdr)))
                 break;
             if (lane == 0) {
@@ -355,8 +396,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
             ++unit_it;
-            for (int s = 0; s < x.ni && ok; ++s, ++c) {
-                const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
+            StepPos w;
+            for (int s = 0; s < x.ns && ok; ++s, ++c, w.next(x.ni)) {
+                int h, i;
+                unit_step<KV, RUNS>(x, s, w, p, h, i);
                 const int st = c & 1;
                 // Q_i (with its LSE and D rows) into the 2-stage ring
                 if (!(ok = lane0_wait(smem_u32(&sm.q_empty[st]), ((c >> 1) & 1) ^ 1, abort_flag,
@@ -366,7 +409,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(qbar, Cfg::kTileBytes);
                     for (int cb = 0; cb < Cfg::kBoxes; ++cb)
-                        tma_load_3d(smem_u32(sm.q[st]) + cb * 16384, &p.tm_q, qbar, cb * 64, x.h,
+                        tma_load_3d(smem_u32(sm.q[st]) + cb * 16384, &p.tm_q, qbar, cb * 64, h,
                                     x.t0 + i * kTile);
                 }
 #pragma unroll
@@ -375,7 +418,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const int r = i * kTile + rr;
                     float l2 = 0.f, dv = 0.f;
                     if (r < x.L) {
-                        const size_t at = (size_t)x.h * p.T + (size_t)(x.t0 + r);
+                        const size_t at = (size_t)h * p.T + (size_t)(x.t0 + r);
                         l2 = p.lse[at] * kLog2e;
                         dv = p.D[at];
                     }
@@ -412,15 +455,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(smem_u32(&sm.sched_empty[slot]));
                 ++sched_it;
                 if (unit.x < 0) break;
-                const BUnit x = decode_bunit<KV>(unit, p);
-                for (int s = 0; s < x.ni; ++s, ++c) {
-                    const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
+                const BUnit x = decode_bunit<KV, RUNS>(unit, p);
+                StepPos w;
+                for (int s = 0; s < x.ns; ++s, ++c, w.next(x.ni)) {
+                    int h, i;
+                    unit_step<KV, RUNS>(x, s, w, p, h, i);
                     if (!(ok = wait_or_abort(smem_u32(&sm.do_empty), (c & 1) ^ 1, abort_flag, hdr)))
                         break;
                     const uint32_t dbar = smem_u32(&sm.do_full);
                     mbar_arrive_expect_tx(dbar, Cfg::kTileBytes);
                     for (int cb = 0; cb < Cfg::kBoxes; ++cb)
-                        tma_load_3d(smem_u32(sm.dout) + cb * 16384, &p.tm_do, dbar, cb * 64, x.h,
+                        tma_load_3d(smem_u32(sm.dout) + cb * 16384, &p.tm_do, dbar, cb * 64, h,
                                     x.t0 + i * kTile);
                 }
             }
@@ -465,10 +510,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(smem_u32(&sm.sched_empty[slot]));
                 ++sched_it;
                 if (unit.x < 0) break;
-                const BUnit x = decode_bunit<KV>(unit, p);
+                const BUnit x = decode_bunit<KV, RUNS>(unit, p);
                 if (!(ok = wait_or_abort(smem_u32(&sm.kv_full), unit_it & 1, abort_flag, hdr))) break;
-                if ((!KV || x.ni > 0) && !(ok = issue_s(cnt))) break;
-                for (int s = 0; s < x.ni; ++s, ++cnt) {
+                if ((!KV || x.ns > 0) && !(ok = issue_s(cnt))) break;
+                for (int s = 0; s < x.ns; ++s, ++cnt) {
                     const int st = cnt & 1;
                     const uint32_t qaddr = smem_u32(sm.q[st]);
                     if (!(ok = wait_or_abort(smem_u32(&sm.do_full), cnt & 1, abort_flag, hdr))) break;
@@ -527,7 +572,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // Q(c+1) and dV(c) done with the S columns; dK only accumulates
                     // until the unit ends, so it goes last.
                     {
-                        bool s_done = s + 1 >= x.ni, q_done = false, k_done = false;
+                        bool s_done = s + 1 >= x.ns, q_done = false, k_done = false;
                         const uint64_t t_start = globaltimer();
                         while (!(s_done && q_done && k_done)) {
                             if (!q_done && mbar_test_wait(smem_u32(&sm.ds_ready), cnt & 1) &&
@@ -592,7 +637,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // for the previous unit's dK/dV epilogue.  Wait for it here, or
                     // two such units in a row could put dkv_full two phases ahead of
                     // the epilogue warps, which parity cannot tell apart.
-                    if (x.ni == 0 && unit_it > 0 &&
+                    if (x.ns == 0 && unit_it > 0 &&
                         !(ok = wait_or_abort(smem_u32(&sm.dkv_free), (unit_it - 1) & 1, abort_flag,
                                              hdr)))
                         break;
@@ -627,14 +672,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
             ++sched_it;
             if (unit.x < 0) break;
-            const BUnit x = decode_bunit<KV>(unit, p);
+            const BUnit x = decode_bunit<KV, RUNS>(unit, p);
             // key position c within its sequence: query column r sees it iff
             // r >= c - off (causal) and r < L; a key past the end sees nothing
             const int c = x.j * kTile + rk;
             const int c_off = c - x.off;
             const int L_vis = c < x.Lk ? x.L : 0;  // (KV only)
-            for (int s = 0; s < x.ni; ++s, ++cnt) {
-                const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
+            StepPos w;
+            for (int s = 0; s < x.ns; ++s, ++cnt, w.next(x.ni)) {
+                int h, i;
+                unit_step<KV, RUNS>(x, s, w, p, h, i);
                 const int st = cnt & 1;
                 // visible query columns of this key row: [lo, hi); the warp skips the
                 // mask when every row sees every column
@@ -744,15 +791,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
             ++sched_it;
             if (unit.x < 0) break;
-            const BUnit x = decode_bunit<KV>(unit, p);
-            for (int s = 0; s < x.ni; ++s) {
-                const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
+            const BUnit x = decode_bunit<KV, RUNS>(unit, p);
+            StepPos w;
+            for (int s = 0; s < x.ns; ++s, w.next(x.ni)) {
+                int h, i;
+                unit_step<KV, RUNS>(x, s, w, p, h, i);
                 if (!(ok = wg_wait(smem_u32(&sm.dq_full), cnt & 1, abort_flag, hdr))) break;
                 tc_fence_after();
                 int* sem = nullptr;
                 bool sem_ok = true;
                 if (p.deterministic) {
-                    sem = sems + (size_t)x.h * n_qtiles + tile_off[x.b] + i;
+                    sem = sems + (size_t)h * n_qtiles + tile_off[x.b] + i;
                     if (leader) {
                         sem_ok = sem_wait(sem, dq_rank<KV>(x, i, p.causal), hdr);
                         if (!sem_ok) raise_abort(abort_flag, hdr, kErrTimeout);
@@ -791,12 +840,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         named_bar_sync(1, 128);
                         if (leader && sem_ok)
                             tma_reduce_add_3d(&p.tm_dq_acc, stage_base + sl * (kTile * 128), cc * 32,
-                                              x.h, x.t0 + row0);
+                                              h, x.t0 + row0);
                         if (leader) bulk_commit_group();
                     }
                 } else if (qr < x.L && sem_ok) {
                     // Ragged last tile of a sequence: per-row vector reductions.
-                    float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + x.h) * DR;
+                    float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + h) * DR;
 #pragma unroll
                     for (int cc = 0; cc < DR / 32; ++cc)
 #pragma unroll
@@ -820,14 +869,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!sem_ok) { ok = false; break; }
             }
             if (!ok) break;
-            // dK_j (times scale) and dV_j for this query head
+            // dK_j (times scale) and dV_j, summed over the unit's query heads
             if (!(ok = wg_wait(smem_u32(&sm.dkv_full), unit_it & 1, abort_flag, hdr))) break;
             tc_fence_after();
             const int kr = x.j * kTile + rr;
             const bool valid = kr < x.Lk;
             const size_t tok = (size_t)x.tk0 + (size_t)kr;
-            const bool none = KV && x.ni == 0;  // no query: dK = dV = 0, TMEM not written
-            const bool gqa = p.Hq != p.Hkv;
+            const bool none = KV && x.ns == 0;  // no query: dK = dV = 0, TMEM not written
+            const bool partial = p.nchunks > 1;  // other units cover the group's other heads
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 const uint32_t col = which == 0 ? Cfg::kColDK : Cfg::kColDV;
@@ -842,8 +891,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = 0u;
                     }
-                    if (gqa) {
-                        float* acc = (which == 0 ? dk_acc : dv_acc) + (tok * p.Hq + x.h) * DR + cc * 32;
+                    if (partial) {
+                        float* acc = (which == 0 ? dk_acc : dv_acc) +
+                                     (tok * (size_t)(p.Hkv * p.nchunks) + x.uh) * DR + cc * 32;
                         float4* d4 = reinterpret_cast<float4*>(acc);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
@@ -958,21 +1008,21 @@ __global__ void __launch_bounds__(256)
     for (long long si = tid; si < n_sems; si += (long long)gridDim.x * blockDim.x) sems[si] = 0;
 }
 
-// dq = scale * dq_acc; for GQA, dk/dv[t,g] = sum over the group's query heads h
-// (in increasing h) of the per-head partials.  One flat index space of float4
-// groups: [0, nq) dq, [nq, nq+nkv) dk, [nq+nkv, nq+2nkv) dv.
+// dq = scale * dq_acc; when the query heads of a key/value head are split over
+// several runs, dk/dv[t,g] = sum over the runs (in increasing order) of their
+// fp32 partials [t, g * nruns + run].  One flat index space of float4 groups:
+// [0, nq) dq, [nq, nq+nkv) dk, [nq+nkv, nq+2nkv) dv.
 template <int D, bool F32>
 __global__ void __launch_bounds__(256)
     bwd_postprocess_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq,
                            const float* __restrict__ dk_acc, const float* __restrict__ dv_acc,
                            void* __restrict__ dk, void* __restrict__ dv, int Tq, int Tk, int Hq,
-                           int Hkv, float scale) {
+                           int Hkv, int nruns, float scale) {
     pdl_begin();
     constexpr int V = D / 4;  // float4 groups per row
     const long long nq = (long long)Tq * Hq * V;
     const long long nkv = dk_acc ? (long long)Tk * Hkv * V : 0;
     const long long stride = (long long)gridDim.x * blockDim.x;
-    const int grp = Hq / Hkv;
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nq + 2 * nkv;
          e += stride) {
         float4 r;
@@ -992,8 +1042,8 @@ __global__ void __launch_bounds__(256)
             const int g = (int)(row % Hkv);
             const float4* src = reinterpret_cast<const float4*>(is_v ? dv_acc : dk_acc);
             r = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int hh = 0; hh < grp; ++hh) {
-                const float4 a = src[(t * Hq + (long long)g * grp + hh) * V + c4];
+            for (int u = 0; u < nruns; ++u) {
+                const float4 a = src[(t * ((long long)Hkv * nruns) + (long long)g * nruns + u) * V + c4];
                 r.x += a.x; r.y += a.y; r.z += a.z; r.w += a.w;
             }
             out = is_v ? dv : dk;
@@ -1016,11 +1066,15 @@ int grid_for(long long work, int threads, int num_sms) {
 
 template <int D, int DR>
 cudaError_t launch_bwd_t(const BwdParams& p, int num_sms, cudaStream_t stream) {
-    auto kern = p.kv ? fa_bwd_kernel<D, DR, true> : fa_bwd_kernel<D, DR, false>;
+    auto kern = p.kv ? (p.hchunk > 1 ? fa_bwd_kernel<D, DR, true, true>
+                                     : fa_bwd_kernel<D, DR, true, false>)
+                     : (p.hchunk > 1 ? fa_bwd_kernel<D, DR, false, true>
+                                     : fa_bwd_kernel<D, DR, false, false>);
     const size_t smem = sizeof(BwdSmem<D>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long long bound = max_tiles(p.B, p.Tk, kTile) * p.Hq;  // units are key/value tiles
+    // units are (key/value tile, run of query heads)
+    const long long bound = max_tiles(p.B, p.Tk, kTile) * (long long)p.Hkv * p.nchunks;
     const int grid = (int)(bound < num_sms ? bound : num_sms);
     if (grid <= 0) return cudaSuccess;
     return launch_pdl(kern, dim3(grid), dim3(kBwdThreads), smem, stream, p);
@@ -1058,14 +1112,14 @@ cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream) {
 
 cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const float* dk_acc,
                                    const float* dv_acc, void* dk, void* dv, int Tq, int Tk,
-                                   int Hq, int Hkv, int d, float scale, int grad_fp32,
+                                   int Hq, int Hkv, int nruns, int d, float scale, int grad_fp32,
                                    int num_sms, cudaStream_t stream) {
     const long long work = ((long long)Tq * Hq + (dk_acc ? 2LL * Tk * Hkv : 0)) * d / 4;
     const int grid = grid_for(work, 256, num_sms);
     cudaError_t e;
 #define FA_POST(DD, FF)                                                                   \
     e = launch_pdl(bwd_postprocess_kernel<DD, FF>, dim3(grid), dim3(256), 0, stream, dq_acc, dq, \
-                   dk_acc, dv_acc, dk, dv, Tq, Tk, Hq, Hkv, scale)
+                   dk_acc, dv_acc, dk, dv, Tq, Tk, Hq, Hkv, nruns, scale)
     if (d == 128) {
         if (grad_fp32) FA_POST(128, true); else FA_POST(128, false);
     } else if (d == 96) {

@@ -89,27 +89,45 @@ __host__ __device__ inline FwdWs fwd_ws_layout(int B, int Hq, int T) {
     return w;
 }
 
+// Backward units walk a run of C query heads of one key/value head ("FlashAttention-
+// 4反向传播优化" section 5.2), accumulating dK and dV over them on chip: C is
+// the largest divisor of the group size Hq / Hkv up to 4 that still leaves
+// kMinBwdUnits units (Hq / C heads' worth of key/value tiles), so that the
+// persistent grid stays balanced; 1 for MHA.
+constexpr long long kMinBwdUnits = 512;
+
+__host__ __device__ inline int bwd_head_run(int Hq, int Hkv, int Tk) {
+    const int grp = Hq / Hkv;
+    for (int c = 4; c > 1; --c)
+        if (grp % c == 0 && (long long)(Hq / c) * cdiv(Tk, kTile) >= kMinBwdUnits) return c;
+    return 1;
+}
+
 // Backward workspace: header | unit list (int2) | per-sequence query-tile
 // offsets (int[B+1]) | semaphores (int[Hq * max_qtiles]) | dQ accumulator
-// fp32 [Tq,Hq,d] | (GQA only) dK and dV partials fp32 [Tk,Hq,d].  Units are
-// key/value tiles (Tk tokens); dQ tiles and semaphores are query tiles (Tq).
+// fp32 [Tq,Hq,d] | (when a group's heads take several runs) dK and dV
+// partials fp32 [Tk, Hkv * runs, d].  Units are key/value tiles (Tk tokens)
+// times runs of heads; dQ tiles and semaphores are query tiles (Tq).
 struct BwdWs {
     size_t units, tile_off, sems, dq_acc, dk_acc, dv_acc, bytes;
     long long max_units, max_qtiles;
+    int hchunk, nruns;  // heads per run, runs per key/value head
 };
 
 __host__ __device__ inline BwdWs bwd_ws_layout(int B, int Hq, int Hkv, int Tq, int Tk, int d) {
     BwdWs w;
+    w.hchunk = bwd_head_run(Hq, Hkv, Tk);
+    w.nruns = (Hq / Hkv) / w.hchunk;
     w.max_qtiles = max_tiles(B, Tq, kTile);
-    w.max_units = max_tiles(B, Tk, kTile) * (long long)Hq;
+    w.max_units = max_tiles(B, Tk, kTile) * (long long)Hkv * w.nruns;
     w.units = kAlign;
     w.tile_off = align_up(w.units + (size_t)w.max_units * 8, kAlign);
     w.sems = align_up(w.tile_off + (size_t)(B + 1) * 4, kAlign);
     w.dq_acc = align_up(w.sems + (size_t)w.max_qtiles * (size_t)Hq * 4, kAlign);
     const size_t acc_q = (size_t)Tq * (size_t)Hq * (size_t)d * 4;
-    const size_t acc_k = (size_t)Tk * (size_t)Hq * (size_t)d * 4;
+    const size_t acc_k = (size_t)Tk * (size_t)Hkv * (size_t)w.nruns * (size_t)d * 4;
     w.dk_acc = align_up(w.dq_acc + acc_q, kAlign);
-    if (Hq != Hkv) {
+    if (w.nruns > 1) {
         w.dv_acc = align_up(w.dk_acc + acc_k, kAlign);
         w.bytes = align_up(w.dv_acc + acc_k, kAlign);
     } else {

@@ -41,6 +41,8 @@ struct BwdParams {
     int causal;
     int deterministic;
     int grad_fp32;
+    int hchunk;                    // query heads one unit walks (bwd_head_run)
+    int nchunks;                   // runs of heads per key/value head: (Hq / Hkv) / hchunk
     const int* cu_seqlens_k;       // key/value sequences; null for dense
     int Nk, Tk;                    // key/value length bound and tokens
     int kv;                        // key boundaries differ from the query ones
@@ -69,9 +71,11 @@ cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, f
 
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream);
 
+// dk_acc/dv_acc: fp32 partials [Tk, Hkv * nruns, d] to sum per key/value head,
+// or null when each unit wrote final dK/dV.
 cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const float* dk_acc,
                                    const float* dv_acc, void* dk, void* dv, int Tq, int Tk,
-                                   int Hq, int Hkv, int d, float scale, int grad_fp32,
+                                   int Hq, int Hkv, int nruns, int d, float scale, int grad_fp32,
                                    int num_sms, cudaStream_t stream);
 
 }  // namespace fa

@@ -48,9 +48,23 @@ def test_workspace_sizes(L):
     T, Hq, d = 4 * 2048, 16, 128
     w = fa.fa_bwd_workspace_size(4, Hq, Hq, 2048, 0, d)
     assert w >= T * Hq * d * 4
-    # GQA adds fp32 dK and dV partials per query head
+    # A backward unit walks a run of up to 4 query heads of one key/value head
+    # (the largest divisor of the group that leaves >= 512 units) and sums
+    # dK/dV over them on chip; fp32 partials [T, Hkv * runs, d] exist only
+    # when a group takes more than one run.
+    # GQA-4 with one run per group (16/4 heads x 64 tiles = 256 units < 512
+    # for runs of 4, so runs of 2): 2 runs per key/value head -> partials
     wg = fa.fa_bwd_workspace_size(4, Hq, 4, 2048, 0, d)
-    assert wg >= w + 2 * T * Hq * d * 4
+    # (its unit list is shorter than MHA's: 8 runs of heads per tile, not 16)
+    assert abs((wg - w) - 2 * T * (4 * 2) * d * 4) < (1 << 16)
+    # the GQA-8 workload (B2 Hq32 Hkv8 N8192): runs of 4 cover each group, no partials
+    w8 = fa.fa_bwd_workspace_size(2, 32, 8, 8192, 0, d)
+    w32 = fa.fa_bwd_workspace_size(2, 32, 32, 8192, 0, d)
+    assert w8 <= w32 < w8 + (1 << 20)   # (a shorter unit list, nothing more)
+    # the MQA workload: 32 heads in runs of 4 -> 8 runs, partials [T, 8, d] x 2
+    w1 = fa.fa_bwd_workspace_size(2, 32, 1, 8192, 0, d)
+    assert w1 - w8 >= 2 * 2 * 8192 * 8 * d * 4
+    assert w1 - w8 < 2 * 2 * 8192 * 8 * d * 4 + (1 << 20)
     off = fa.fa_bwd_workspace_semaphore_offset(4, Hq, Hq, 2048, 0, d)
     assert 0 < off < w and off % 256 == 0
     assert fa.fa_bwd_workspace_size(1, 4, 4, 16, 0, 256) == 0  # unsupported head dim

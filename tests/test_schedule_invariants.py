@@ -12,7 +12,8 @@ That is deadlock-free at any size only if, for every dQ tile,
 This test restates the schedule (the scheduler's descending key/value-tile
 order, each unit's walk and rank) from its definition in the kernels'
 comments and checks both properties.  An earlier cyclic non-causal order
-broke property 2.
+broke property 2.  A unit may walk a run of C query heads of one key/value
+head, one after the other; the properties must hold for every run length.
 """
 import itertools
 import random
@@ -66,16 +67,21 @@ def rank(j, i, lq, lk, causal):
     return jmax - j
 
 
-def check(lq_list, lk_list, H, causal):
-    order = unit_order(lk_list, H)
+def check(lq_list, lk_list, H, causal, run=1):
+    """H query heads in runs of `run` heads per unit (heads of one run walked
+    one after the other)."""
+    assert H % run == 0
+    order = unit_order(lk_list, H // run)
     pos = {u: p for p, u in enumerate(order)}
     contributions = {}  # (b, h, i) -> [(rank, position, j)]
-    for (b, j, h), p in pos.items():
+    for (b, j, u), p in pos.items():
         lq, lk = lq_list[b], lk_list[b]
         _, _, _, _, ni = unit_geometry(j, lq, lk, causal)
-        for s in range(ni):
-            i = walk(j, s, lq, lk, causal)
-            contributions.setdefault((b, h, i), []).append((rank(j, i, lq, lk, causal), p, j))
+        for h in range(u * run, (u + 1) * run):
+            for s in range(ni):
+                i = walk(j, s, lq, lk, causal)
+                contributions.setdefault((b, h, i), []).append(
+                    (rank(j, i, lq, lk, causal), p, j))
     for key, cs in contributions.items():
         ranks = sorted(r for r, _, _ in cs)
         assert ranks == list(range(len(cs))), (key, ranks)
@@ -95,10 +101,11 @@ def check(lq_list, lk_list, H, causal):
             assert got == want, (b, i, sorted(want), sorted(got))
 
 
+@pytest.mark.parametrize("run", [1, 2, 4])
 @pytest.mark.parametrize("causal", [False, True])
-def test_equal_lengths(causal):
+def test_equal_lengths(causal, run):
     for lengths in ([2048] * 4, [1, 127, 128, 129, 300, 4097], [32768]):
-        check(lengths, lengths, 2, causal)
+        check(lengths, lengths, 4, causal, run)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -108,6 +115,7 @@ def test_different_lengths(causal):
              ([0, 50, 128], [200, 0, 128])]
     for lq, lk in cases:
         check(lq, lk, 2, causal)
+        check(lq, lk, 4, causal, run=2)
 
 
 def test_random_geometries():
