@@ -143,9 +143,10 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, fa_dty
  * Workspace of the backward pass (fa_bwd_preprocess + fa_bwd), in bytes: a
  * header (device error word, work counter), the scheduler's ordered unit list
  * and per-sequence tile offsets, one semaphore per (query head, query tile)
- * for deterministic mode, the fp32 dQ accumulator [T,Hq,d], and -- when
- * Hq != Hkv -- fp32 per-query-head dK/dV partials [T,Hq,d] each.
- * Returns 0 for invalid sizes.
+ * for deterministic mode, the fp32 dQ accumulator [T,Hq,d], and -- when the
+ * query heads of a key/value head take more than one backward unit (a unit
+ * walks a run of up to 4 of them, summing their dK/dV on chip) -- fp32 dK/dV
+ * partials [T, Hkv * runs, d] each.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int N, int total_tokens, int d);
 
