@@ -50,3 +50,23 @@ def _workload_args():
 
 def test_reference_arm_other_rank_is_silent():
     assert _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
+
+
+def test_traffic_figure_is_tied_to_the_kernel_sources(monkeypatch):
+    """roofline.traffic is the recorded DRAM bytes only while the backward's
+    sources are the ones the capture was taken on; otherwise null."""
+    import bench
+    sha = bench.sources_sha()
+    monkeypatch.setattr(bench, "FA_BWD_DRAM", {"mid_causal": {"bytes": 1.0e9, "sources": sha}})
+    assert bench.bwd_traffic("mid_causal") == 1.0e9
+    assert bench.bwd_traffic("long_causal") is None
+    monkeypatch.setattr(bench, "FA_BWD_DRAM",
+                        {"mid_causal": {"bytes": 1.0e9, "sources": "0" * 16}})
+    assert bench.bwd_traffic("mid_causal") is None
+
+
+def test_steps_for_fills_the_clock_window():
+    import bench
+    # a 0.34 ms step plus the flush: about 2 s of steps
+    assert 4000 <= bench.steps_for(0.34, 2.0, lo=200) <= 5000
+    assert bench.steps_for(100.0, 1.0, lo=10) == 10
