@@ -37,7 +37,7 @@ if ROOT not in sys.path:
 import synth  # noqa: E402  (input generator: no attention arithmetic)
 
 METRIC = "attention fwd+bwd BF16 TFLOPs/s (hd128, causal) and % of GB300 dense BF16 peak"
-# --forward-only (head dimensions 192 and 256 have no backward)
+# --forward-only: the forward alone
 METRIC_FWD = "attention fwd BF16 TFLOPs/s and % of GB300 dense BF16 peak"
 
 # DRAM bytes (read + write) of one fa_bwd call -- the backward kernel and its

@@ -192,7 +192,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, fa_dtyp
 size_t bwd_ws_bytes(int B, int Hq, int Hkv, int Nq, int total_q, int Nk, int total_k, int d,
                     bool sems_offset) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || total_q < 0 || Nk < 0 || total_k < 0 ||
-        (d != 64 && d != 96 && d != 128))
+        (d != 64 && d != 96 && d != 128 && d != 192 && d != 256))
         return 0;
     const long long Tq = total_q > 0 ? total_q : (long long)B * Nq;
     const long long Tk = total_k > 0 ? total_k : (long long)B * Nk;
@@ -209,7 +209,6 @@ fa_status bwd_preprocess_impl(const void* o, fa_dtype o_dtype, const void* dout,
     Shape s;
     fa_status st = check_shape(B, Hq, Hkv, Nq, total_q, Nk, total_k, d, cu_q, cu_k, s);
     if (st != FA_OK) return st;
-    if (d > 128) return FA_ERR_UNSUPPORTED;  // the backward keeps 256 + 2d TMEM columns
     if (o_dtype != FA_BF16 && o_dtype != FA_FP32) return FA_ERR_INVALID_ARG;
     if (s.Tq == 0 || s.Tk == 0 || B == 0) return FA_OK;  // fa_bwd needs no workspace then
     if (!sched_fits(s, Nk, kTile)) return FA_ERR_UNSUPPORTED;  // units are key/value tiles
@@ -246,7 +245,6 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* dout
     Shape s;
     fa_status st = check_shape(B, Hq, Hkv, Nq, total_q, Nk, total_k, d, cu_q, cu_k, s);
     if (st != FA_OK) return st;
-    if (d > 128) return FA_ERR_UNSUPPORTED;  // the backward keeps 256 + 2d TMEM columns
     if (grad_dtype != FA_BF16 && grad_dtype != FA_FP32) return FA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_UNSUPPORTED;
     if (B == 0 || (s.Tq == 0 && s.Tk == 0)) return FA_OK;

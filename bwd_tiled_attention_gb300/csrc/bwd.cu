@@ -948,6 +948,444 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- head dimensions 192 and 256
+//
+// S, dP, dK and dV of one key/value tile need 256 + 2d TMEM columns, more than
+// the 512 there are above d = 128, and K, V, Q and dO tiles of 48-64 KB each do
+// not fit shared memory together.  So a unit (one key/value tile of one
+// sequence and query head) walks its query tiles twice:
+//   pass 1: S^T = K Q^T, P^T (bf16, in TMEM over S^T), dV += P^T dO;
+//   pass 2: S^T and dP^T = V dO^T, dS^T = P^T (dP^T - D) (bf16, shared memory),
+//           dK += dS^T Q, dQ = dS K into the columns S^T and dP^T held.
+// dV is stored after pass 1 and dK after pass 2, from the same TMEM columns
+// [256, 256 + d).  K and V stay in shared memory for the unit; Q and dO are
+// streamed in 64-column chunks through a 4-slot ring, loaded two chunks ahead
+// of the MMA that reads them (pass 1 reads Q, dO; pass 2 reads Q, dO, Q), so
+// pass 2 recomputes S and the MMA work is 1.2 times the five products.  One
+// thread issues every load and MMA; all 128 threads (one per key row, or one
+// per query row in the dQ merge) do the elementwise work between them, and
+// every hand-off is a bounded mbarrier wait or a block barrier.  dQ is merged
+// with per-row fp32 vector reductions, ordered by the same semaphores as the
+// main kernel in deterministic mode.
+constexpr int kWideThreads = 128;
+constexpr int kWideSlots = 4;    // ring of 64-column Q/dO chunks
+constexpr int kWideAhead = 2;    // chunks loaded ahead of the one an MMA reads
+constexpr int kWideChunkBytes = kTile * 64 * 2;
+
+template <int D>
+struct WideSmem {
+    alignas(1024) uint8_t k[kTile * D * 2];
+    alignas(1024) uint8_t v[kTile * D * 2];
+    alignas(1024) uint8_t ring[kWideSlots][kWideChunkBytes];
+    alignas(1024) uint8_t ds[kTile * kTile * 2];  // dS^T, two 64-column boxes, 128B-swizzled
+    alignas(16) float lse2[kTile];
+    alignas(16) float dd[kTile];
+    alignas(8) uint64_t kv_full, mma_done, drain;
+    uint64_t slot_full[kWideSlots], slot_free[kWideSlots];
+    int2 unit;
+    uint32_t tmem_base;
+    int abort_flag;
+    int zero;
+};
+static_assert(sizeof(WideSmem<256>) <= 232448, "wide backward shared memory exceeds 227 KB");
+
+template <int D, bool KV>
+__global__ void __launch_bounds__(kWideThreads, 1)
+    fa_bwd_wide_kernel(const __grid_constant__ BwdParams p) {
+    pdl_trigger();
+    constexpr int C = D / 64;                       // 64-column chunks of a row
+    constexpr uint32_t kColDKV = 256;               // dV (pass 1), then dK (pass 2)
+    constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idN = make_idesc_bf16(128, 64, false, true);
+    constexpr uint32_t idDQ = make_idesc_bf16(128, D, true, true);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(p.workspace);
+    if (smem_u32(smem_raw) & 1023u) {
+        pdl_wait();
+        if (threadIdx.x == 0) atomicOr(&hdr->error, kErrSmemAlign);
+        return;
+    }
+    WideSmem<D>& sm = *reinterpret_cast<WideSmem<D>*>(smem_raw);
+    const char* ws = static_cast<const char*>(p.workspace);
+    const int2* units = reinterpret_cast<const int2*>(ws + p.units_off);
+    const int* tile_off = reinterpret_cast<const int*>(ws + p.tile_off_off);
+    int* sems = reinterpret_cast<int*>(static_cast<char*>(p.workspace) + p.sems_off);
+    float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + p.dq_acc_off);
+    float* dk_acc = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + p.dk_acc_off);
+    float* dv_acc = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + p.dv_acc_off);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    volatile int* abort_flag = &sm.abort_flag;
+
+    if (tid == 0) {
+        mbar_init(smem_u32(&sm.kv_full), 1);
+        mbar_init(smem_u32(&sm.mma_done), 1);
+        mbar_init(smem_u32(&sm.drain), 1);
+        for (int s = 0; s < kWideSlots; ++s) {
+            mbar_init(smem_u32(&sm.slot_full[s]), 1);
+            mbar_init(smem_u32(&sm.slot_free[s]), 1);
+        }
+        sm.abort_flag = 0;
+        sm.zero = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&sm.tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    pdl_wait();  // the unit list, LSE, D and the reset workspace are the previous kernels' output
+    const int n_units = hdr->n_units;
+    const int n_qtiles = hdr->n_qtiles;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t kaddr = smem_u32(sm.k), vaddr = smem_u32(sm.v), dsaddr = smem_u32(sm.ds);
+    const uint32_t mbar_mma = smem_u32(&sm.mma_done);
+
+    // Ring state (thread 0): chunks consumed before the current pass, and the
+    // pass's chunks whose loads were issued.
+    int g0 = 0, issued = 0;
+    int mma_waits = 0, kv_waits = 0;  // phases of mma_done / kv_full waited for
+    int kv_issued = 0;                // (thread 0) K/V loads issued
+    // ok changes only right after a block-wide vote (__syncthreads_or), so every
+    // thread takes the same branches around the block barriers.
+    bool ok = true;
+
+    // Every thread waits for the next phase of mma_done.
+    auto wait_mma = [&]() {
+        if (!mbar_wait(mbar_mma, mma_waits & 1, abort_flag)) raise_abort(abort_flag, hdr, kErrTimeout);
+        ++mma_waits;
+        tc_fence_after();
+    };
+
+    while (true) {
+        if (tid == 0) {
+            const int u = atomicAdd(&hdr->counter, 1);
+            sm.unit = u < n_units ? units[u] : make_int2(-1, 0);
+        }
+        __syncthreads();
+        const int2 unit = sm.unit;
+        if (__syncthreads_or(unit.x < 0 || *abort_flag != 0)) break;
+        const BUnit x = decode_bunit<KV, false>(unit, p);
+        const int h = x.h0;
+        // this thread's key row (P, dS phases; dK/dV epilogue): key position c
+        // within its sequence; query column r of tile i sees it iff it is in [lo, hi)
+        const int c = x.j * kTile + tid;
+        const int c_off = c - x.off;
+        const int L_vis = c < x.Lk ? x.L : 0;
+        auto visible = [&](int i, int& lo, int& hi) {
+            if constexpr (KV) {
+                lo = p.causal ? max(0, c_off - i * kTile) : 0;
+                hi = min(kTile, L_vis - i * kTile);
+            } else {
+                lo = p.causal ? max(0, c - i * kTile) : 0;
+                hi = c < x.L ? min(kTile, x.L - i * kTile) : 0;
+            }
+        };
+        // LSE (base 2) and D of query tile i's rows into shared memory
+        auto load_rows = [&](int i) {
+            const int q = i * kTile + tid;
+            float l2 = 0.f, dv = 0.f;
+            if (q < x.L) {
+                const size_t at = (size_t)h * p.T + (size_t)(x.t0 + q);
+                l2 = p.lse[at] * kLog2e;
+                dv = p.D[at];
+            }
+            sm.lse2[tid] = l2;
+            sm.dd[tid] = dv;
+        };
+
+        if (tid == 0) {
+            const uint32_t bar = smem_u32(&sm.kv_full);
+            mbar_arrive_expect_tx(bar, 2 * kTile * D * 2);
+            for (int cb = 0; cb < C; ++cb) {
+                tma_load_3d(kaddr + cb * 16384, &p.tm_k, bar, cb * 64, x.g, x.tk0 + x.j * kTile);
+                tma_load_3d(vaddr + cb * 16384, &p.tm_v, bar, cb * 64, x.g, x.tk0 + x.j * kTile);
+            }
+            ++kv_issued;
+        }
+        if (!mbar_wait(smem_u32(&sm.kv_full), kv_waits & 1, abort_flag))
+            raise_abort(abort_flag, hdr, kErrTimeout);
+        ++kv_waits;
+        if (__syncthreads_or(*abort_flag != 0)) break;
+
+        for (int pass = 0; pass < 2 && ok; ++pass) {
+            const int per = pass == 0 ? 2 * C : 3 * C;  // chunks read per step
+            const int total = x.ns * per;
+            // chunk k of the pass: query tile of step k / per; Q columns, then dO
+            // columns, then (pass 2) Q columns again
+            auto issue_upto = [&](int kmax) -> bool {
+                kmax = min(kmax, total);
+                while (issued < kmax) {
+                    const int k = issued, g = g0 + k;
+                    const int slot = g % kWideSlots, n = g / kWideSlots;
+                    if (n > 0 && !mbar_wait(smem_u32(&sm.slot_free[slot]), (n - 1) & 1, abort_flag)) {
+                        raise_abort(abort_flag, hdr, kErrTimeout);
+                        return false;
+                    }
+                    const int s = k / per, w = k - s * per;
+                    const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
+                    const bool is_do = w >= C && w < 2 * C;
+                    const int col = (w % C) * 64;
+                    const uint32_t bar = smem_u32(&sm.slot_full[slot]);
+                    mbar_arrive_expect_tx(bar, kWideChunkBytes);
+                    tma_load_3d(smem_u32(sm.ring[slot]), is_do ? &p.tm_do : &p.tm_q, bar, col, h,
+                                x.t0 + i * kTile);
+                    ++issued;
+                }
+                return true;
+            };
+            // thread 0: wait for chunk k (issuing loads ahead); returns its address or 0
+            auto acquire = [&](int k) -> uint32_t {
+                if (!issue_upto(k + 1 + kWideAhead)) return 0u;
+                const int g = g0 + k;
+                if (!mbar_wait(smem_u32(&sm.slot_full[g % kWideSlots]), (g / kWideSlots) & 1,
+                               abort_flag)) {
+                    raise_abort(abort_flag, hdr, kErrTimeout);
+                    return 0u;
+                }
+                tc_fence_after();
+                return smem_u32(sm.ring[g % kWideSlots]);
+            };
+            auto release = [&](int k) {
+                mma_commit(smem_u32(&sm.slot_free[(g0 + k) % kWideSlots]));
+            };
+
+            for (int s = 0; s < x.ns; ++s) {
+                const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
+                load_rows(i);
+                __syncthreads();
+                // S^T = K Q_i^T into [0, 128); pass 2 also dP^T = V dO_i^T into [128, 256)
+                if (tid == 0) {
+                    for (int cc = 0; cc < C; ++cc) {
+                        const uint32_t a = acquire(s * per + cc);
+                        if (!a) break;  // (abort flag raised: every thread stops below)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem, make_sdesc(kaddr + cc * 16384 + kk * 32, 16, 1024),
+                                   make_sdesc(a + kk * 32, 16, 1024), idS, (cc | kk) > 0);
+                        release(s * per + cc);
+                    }
+                    for (int cc = 0; pass == 1 && cc < C; ++cc) {
+                        const uint32_t a = acquire(s * per + C + cc);
+                        if (!a) break;  // (abort flag raised: every thread stops below)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + 128, make_sdesc(vaddr + cc * 16384 + kk * 32, 16, 1024),
+                                   make_sdesc(a + kk * 32, 16, 1024), idS, (cc | kk) > 0);
+                        release(s * per + C + cc);
+                    }
+                    mma_commit(mbar_mma);
+                }
+                wait_mma();
+                int lo, hi;
+                visible(i, lo, hi);
+                const bool full = lo == 0 && hi == kTile;
+                if (pass == 0) {
+                    // P^T of this key row, bf16, packed over the first 32 columns of
+                    // each 64-column half of S^T (query columns [64h + 16m, +16) in
+                    // TMEM columns [64h + 8m, +8)): the A operand of dV
+                    uint32_t sv[4][32];
+#pragma unroll
+                    for (int qc = 0; qc < 4; ++qc) tmem_ld32(tmem + lane_off + qc * 32, sv[qc]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int qc = 0; qc < 4; ++qc) {
+                        uint32_t pk[16];
+                        if (full)
+                            p_chunk<false>(sv[qc], sm.lse2 + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                        else
+                            p_chunk<true>(sv[qc], sm.lse2 + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                        tmem_st16(tmem + lane_off + (qc >> 1) * 64 + (qc & 1) * 16, pk);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    if (__syncthreads_or(*abort_flag != 0)) { ok = false; break; }
+                    // dV += P^T dO_i, 64 columns of dO per chunk
+                    if (tid == 0) {
+                        tc_fence_after();
+                        for (int cc = 0; cc < C; ++cc) {
+                            const uint32_t a = acquire(s * per + C + cc);
+                            if (!a) break;  // (abort flag raised: every thread stops below)
+#pragma unroll
+                            for (int kk = 0; kk < kTile / 16; ++kk)
+                                mma_ts(tmem + kColDKV + cc * 64, tmem + (kk >> 2) * 64 + (kk & 3) * 8,
+                                       make_sdesc(a + kk * 2048, 16384, 1024), idN,
+                                       (s > 0 || kk > 0) ? 1u : 0u);
+                            release(s * per + C + cc);
+                        }
+                        mma_commit(mbar_mma);
+                    }
+                    wait_mma();  // dV read P^T: the next S may overwrite it
+                    if (__syncthreads_or(*abort_flag != 0)) { ok = false; break; }
+                    continue;
+                }
+                // pass 2: dS^T = P^T (dP^T - D), bf16, swizzled rows of the dS^T tile
+                uint8_t* ds_row = sm.ds + tid * 128;
+                const int sw = tid & 7;
+#pragma unroll 1
+                for (int qc = 0; qc < 4; ++qc) {
+                    uint32_t sv[32], dv[32];
+                    tmem_ld32(tmem + lane_off + qc * 32, sv);
+                    tmem_ld32(tmem + lane_off + 128 + qc * 32, dv);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+                    if (full)
+                        p_chunk<false>(sv, sm.lse2 + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                    else
+                        p_chunk<true>(sv, sm.lse2 + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                    uint32_t out[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 pf =
+                            __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[e]));
+                        const float d0 = sm.dd[qc * 32 + 2 * e], d1 = sm.dd[qc * 32 + 2 * e + 1];
+                        out[e] = pack_bf16x2(pf.x * (__uint_as_float(dv[2 * e]) - d0),
+                                             pf.y * (__uint_as_float(dv[2 * e + 1]) - d1));
+                    }
+                    // 32 query columns = 4 chunks of 16 bytes of half (qc >> 1)'s block
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int ch = (qc & 1) * 4 + e;
+                        *reinterpret_cast<uint4*>(ds_row + (qc >> 1) * 16384 + ((ch ^ sw) << 4)) =
+                            make_uint4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                if (__syncthreads_or(*abort_flag != 0)) { ok = false; break; }
+                if (tid == 0) {
+                    tc_fence_after();
+                    // dK += dS^T Q_i, 64 columns of Q per chunk (A = dS^T, K-major)
+                    for (int cc = 0; cc < C; ++cc) {
+                        const uint32_t a = acquire(s * per + 2 * C + cc);
+                        if (!a) break;  // (abort flag raised: every thread stops below)
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ss(tmem + kColDKV + cc * 64,
+                                   make_sdesc(dsaddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                                   make_sdesc(a + kk * 2048, 16384, 1024), idN,
+                                   (s > 0 || kk > 0) ? 1u : 0u);
+                        release(s * per + 2 * C + cc);
+                    }
+                    // dQ = dS K_j into [0, D): S^T and dP^T have been read
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ss(tmem, make_sdesc(dsaddr + kk * 2048, 16384, 1024),
+                               make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ, kk > 0);
+                    mma_commit(mbar_mma);
+                }
+                wait_mma();
+                // dQ merge: this thread's query row of tile i
+                int* sem = nullptr;
+                if (p.deterministic) {
+                    sem = sems + (size_t)h * n_qtiles + tile_off[x.b] + i;
+                    if (tid == 0 && !sem_wait(sem, dq_rank<KV>(x, i, p.causal), hdr))
+                        raise_abort(abort_flag, hdr, kErrTimeout);
+                }
+                if (__syncthreads_or(*abort_flag != 0)) { ok = false; break; }
+                const int qr = i * kTile + tid;
+                float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + h) * D;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + cc * 32, v);
+                    tmem_ld_wait();
+                    if (qr < x.L) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[4 * e]),
+                                       __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
+                                       __uint_as_float(v[4 * e + 3]));
+                    }
+                }
+                tc_fence_before();
+                if (p.deterministic) __threadfence();  // this contribution before the next one
+                __syncthreads();
+                if (p.deterministic && tid == 0) red_release_gpu_add(sem, 1);
+            }
+            if (!ok) break;
+            // epilogue of the pass: dV (pass 1) or dK times scale (pass 2) of this key row
+            const bool valid = c < x.Lk;
+            const size_t tok = (size_t)x.tk0 + (size_t)c;
+            const bool none = x.ns == 0;  // (KV) no query sees the tile: zeros, TMEM not written
+            const float mul = pass == 0 ? 1.f : p.scale;
+            const bool partial = p.nchunks > 1;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + kColDKV + cc * 32, v);
+                tmem_ld_wait();
+                if (!valid) continue;
+                if (none) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                if (partial) {
+                    float* acc = (pass == 0 ? dv_acc : dk_acc) +
+                                 (tok * (size_t)(p.Hkv * p.nchunks) + x.uh) * D + cc * 32;
+                    float4* d4 = reinterpret_cast<float4*>(acc);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul,
+                                            __uint_as_float(v[4 * e + 1]) * mul,
+                                            __uint_as_float(v[4 * e + 2]) * mul,
+                                            __uint_as_float(v[4 * e + 3]) * mul);
+                } else if (p.grad_fp32) {
+                    float* out = static_cast<float*>(pass == 0 ? p.dv : p.dk) +
+                                 (tok * p.Hkv + x.g) * D + cc * 32;
+                    float4* d4 = reinterpret_cast<float4*>(out);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul,
+                                            __uint_as_float(v[4 * e + 1]) * mul,
+                                            __uint_as_float(v[4 * e + 2]) * mul,
+                                            __uint_as_float(v[4 * e + 3]) * mul);
+                } else {
+                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(pass == 0 ? p.dv : p.dk) +
+                                         (tok * p.Hkv + x.g) * D + cc * 32;
+                    uint4* d4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        d4[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]) * mul,
+                                                       __uint_as_float(v[8 * e + 1]) * mul),
+                                           pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul,
+                                                       __uint_as_float(v[8 * e + 3]) * mul),
+                                           pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul,
+                                                       __uint_as_float(v[8 * e + 5]) * mul),
+                                           pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul,
+                                                       __uint_as_float(v[8 * e + 7]) * mul));
+                }
+            }
+            tc_fence_before();
+            __syncthreads();  // the dK/dV columns are free for the next pass or unit
+            g0 += total;
+            issued = 0;
+        }
+        if (__syncthreads_or(!ok || *abort_flag != 0)) break;
+    }
+
+    // never leave a TMA write or an MMA in flight, then release TMEM
+    if (tid == 0) {
+        const volatile int* z = &sm.zero;
+        const int last = g0 + issued;  // chunks whose loads were issued
+        for (int e = 0; e < kWideSlots && e < last; ++e) {
+            const int g = last - 1 - e;
+            mbar_wait(smem_u32(&sm.slot_full[g % kWideSlots]), (g / kWideSlots) & 1, z);
+        }
+        if (kv_issued > 0) mbar_wait(smem_u32(&sm.kv_full), (kv_issued - 1) & 1, z);
+        mma_commit(smem_u32(&sm.drain));
+        mbar_wait(smem_u32(&sm.drain), 0, z);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // D = rowsum(dO * O) per (token, head); zero the dQ accumulator row and the
 // semaphores.  Each lane takes 8 elements (16-byte loads), D/8 lanes per row,
 // so a warp covers 32/(D/8) rows per pass.
@@ -957,7 +1395,8 @@ __global__ void __launch_bounds__(256)
                           float* __restrict__ Dout, float* __restrict__ dq_acc,
                           int* __restrict__ sems, long long n_sems, int T, int Hq) {
     pdl_begin();
-    constexpr int LPR = D == 96 ? 16 : D / 8;  // lanes per row (a power of two)
+    // lanes per row (a power of two; lanes past the row idle at D = 96 and 192)
+    constexpr int LPR = D == 96 ? 16 : (D == 192 ? 32 : D / 8);
     constexpr int RPW = 32 / LPR;  // rows per warp pass
     const long long rows = (long long)T * Hq;
     const long long warp_g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -968,7 +1407,7 @@ __global__ void __launch_bounds__(256)
         const long long r = r0 + sub;
         const bool valid = r < rows;
         float acc = 0.f;
-        if (valid && l * 8 < D) {  // (lanes past the row idle when D = 96)
+        if (valid && l * 8 < D) {
             const size_t base = (size_t)r * D + (size_t)l * 8;
             const uint4 dv = *reinterpret_cast<const uint4*>(dout + base);
             const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
@@ -1064,6 +1503,18 @@ int grid_for(long long work, int threads, int num_sms) {
     return (int)(g < 1 ? 1 : g);
 }
 
+template <int D>
+cudaError_t launch_bwd_wide_t(const BwdParams& p, int num_sms, cudaStream_t stream) {
+    auto kern = p.kv ? fa_bwd_wide_kernel<D, true> : fa_bwd_wide_kernel<D, false>;
+    const size_t smem = sizeof(WideSmem<D>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long bound = max_tiles(p.B, p.Tk, kTile) * (long long)p.Hkv * p.nchunks;
+    const int grid = (int)(bound < num_sms ? bound : num_sms);
+    if (grid <= 0) return cudaSuccess;
+    return launch_pdl(kern, dim3(grid), dim3(kWideThreads), smem, stream, p);
+}
+
 template <int D, int DR>
 cudaError_t launch_bwd_t(const BwdParams& p, int num_sms, cudaStream_t stream) {
     auto kern = p.kv ? (p.hchunk > 1 ? fa_bwd_kernel<D, DR, true, true>
@@ -1095,6 +1546,10 @@ cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, f
                    dq_acc, sems, n_sems, T, Hq)
     if (d == 128) {
         if (o_fp32) FA_PRE(128, true); else FA_PRE(128, false);
+    } else if (d == 256) {
+        if (o_fp32) FA_PRE(256, true); else FA_PRE(256, false);
+    } else if (d == 192) {
+        if (o_fp32) FA_PRE(192, true); else FA_PRE(192, false);
     } else if (d == 96) {
         if (o_fp32) FA_PRE(96, true); else FA_PRE(96, false);
     } else {
@@ -1105,6 +1560,8 @@ cudaError_t launch_bwd_preprocess(const void* o, int o_fp32, const void* dout, f
 }
 
 cudaError_t launch_bwd(const BwdParams& p, int num_sms, cudaStream_t stream) {
+    if (p.d == 256) return launch_bwd_wide_t<256>(p, num_sms, stream);
+    if (p.d == 192) return launch_bwd_wide_t<192>(p, num_sms, stream);
     if (p.d == 128) return launch_bwd_t<128, 128>(p, num_sms, stream);
     if (p.d == 96) return launch_bwd_t<128, 96>(p, num_sms, stream);
     return launch_bwd_t<64, 64>(p, num_sms, stream);
@@ -1122,6 +1579,10 @@ cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const float* d
                    dk_acc, dv_acc, dk, dv, Tq, Tk, Hq, Hkv, nruns, scale)
     if (d == 128) {
         if (grad_fp32) FA_POST(128, true); else FA_POST(128, false);
+    } else if (d == 256) {
+        if (grad_fp32) FA_POST(256, true); else FA_POST(256, false);
+    } else if (d == 192) {
+        if (grad_fp32) FA_POST(192, true); else FA_POST(192, false);
     } else if (d == 96) {
         if (grad_fp32) FA_POST(96, true); else FA_POST(96, false);
     } else {

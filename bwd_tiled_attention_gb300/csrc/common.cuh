@@ -93,10 +93,11 @@ __host__ __device__ inline FwdWs fwd_ws_layout(int B, int Hq, int T) {
 // 4反向传播优化" section 5.2), accumulating dK and dV over them on chip: C is
 // the largest divisor of the group size Hq / Hkv up to 4 that still leaves
 // kMinBwdUnits units (Hq / C heads' worth of key/value tiles), so that the
-// persistent grid stays balanced; 1 for MHA.
+// persistent grid stays balanced; 1 for MHA and above d = 128.
 constexpr long long kMinBwdUnits = 512;
 
-__host__ __device__ inline int bwd_head_run(int Hq, int Hkv, int Tk) {
+__host__ __device__ inline int bwd_head_run(int Hq, int Hkv, int Tk, int d) {
+    if (d > 128) return 1;  // the wide-head backward walks one query head per unit
     const int grp = Hq / Hkv;
     for (int c = 4; c > 1; --c)
         if (grp % c == 0 && (long long)(Hq / c) * cdiv(Tk, kTile) >= kMinBwdUnits) return c;
@@ -116,7 +117,7 @@ struct BwdWs {
 
 __host__ __device__ inline BwdWs bwd_ws_layout(int B, int Hq, int Hkv, int Tq, int Tk, int d) {
     BwdWs w;
-    w.hchunk = bwd_head_run(Hq, Hkv, Tk);
+    w.hchunk = bwd_head_run(Hq, Hkv, Tk, d);
     w.nruns = (Hq / Hkv) / w.hchunk;
     w.max_qtiles = max_tiles(B, Tq, kTile);
     w.max_units = max_tiles(B, Tk, kTile) * (long long)Hkv * w.nruns;

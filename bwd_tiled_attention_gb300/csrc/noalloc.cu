@@ -62,7 +62,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                     int Hq, int Hkv, int N, int total_tokens, int d, float scale,
                                     int causal, const int* cu_seqlens, int deterministic,
                                     fa_stream_t stream) {
-    if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128 && d != 192 && d != 256) return FA_ERR_UNSUPPORTED;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || total_tokens < 0) return FA_ERR_INVALID_ARG;
     const long long T = total_tokens > 0 ? (long long)total_tokens : (long long)B * N;
     if (T == 0 || B == 0) return FA_OK;

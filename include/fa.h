@@ -32,13 +32,13 @@
  *   FA_ERR_INVALID_ARG by fa_check_device_status and produces no output).
  * - q, k, v, dout, dq, dk, dv and o must be 16-byte aligned (TMA).
  * - Query head h uses key/value head floor(h * Hkv / Hq); Hq % Hkv == 0.
- * - d must be 64, 96 or 128; the forward calls also take 192 and 256.
- *   96 runs on 128-column tiles whose last 32 columns are zero (at the
- *   tensor-core cost of d = 128).  The forward at 192 and 256 runs one
- *   128-row query tile per work unit; the
- *   backward calls return FA_ERR_UNSUPPORTED above 128, since they keep S,
- *   dP, dK and dV of a tile in tensor memory (256 + 2d of its 512 columns).
- *   Other head dimensions return FA_ERR_UNSUPPORTED.  Inputs are bf16.
+ * - d must be 64, 96, 128, 192 or 256.  96 runs on 128-column tiles whose
+ *   last 32 columns are zero (at the tensor-core cost of d = 128).  The
+ *   forward at 192 and 256 runs one 128-row query tile per work unit.  The
+ *   backward at 192 and 256 walks each key/value tile's query tiles twice
+ *   (dV, then dK and dQ), streaming Q and dO in 64-column chunks, since S,
+ *   dP, dK and dV of a tile would need 256 + 2d of the 512 tensor-memory
+ *   columns.  Other head dimensions return FA_ERR_UNSUPPORTED.  Inputs are bf16.
  *   scale multiplies QK^T (usually
  *   1/sqrt(d)) and must be positive.  causal = 1 hides key j from query i
  *   when j > i (positions within the sequence; queries and keys have equal

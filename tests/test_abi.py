@@ -67,7 +67,8 @@ def test_workspace_sizes(L):
     assert w1 - w8 < 2 * 2 * 8192 * 8 * d * 4 + (1 << 20)
     off = fa.fa_bwd_workspace_semaphore_offset(4, Hq, Hq, 2048, 0, d)
     assert 0 < off < w and off % 256 == 0
-    assert fa.fa_bwd_workspace_size(1, 4, 4, 16, 0, 256) == 0  # unsupported head dim
+    assert fa.fa_bwd_workspace_size(1, 4, 4, 16, 0, 320) == 0  # unsupported head dim
+    assert fa.fa_bwd_workspace_size(1, 4, 4, 16, 0, 256) > 0   # 192 and 256: the wide backward
     assert fa.fa_bwd_workspace_size(1, 4, 4, 16, 0, 96) > 0    # 96 runs on 128-column tiles
 
 
@@ -117,8 +118,9 @@ def bwd_call(**kw):
 def test_bwd_rejects_bad_arguments(L):
     assert bwd_call(Hkv=3) == fa.FA_ERR_INVALID_ARG
     assert bwd_call(d=32) == fa.FA_ERR_UNSUPPORTED
-    assert bwd_call(d=256) == fa.FA_ERR_UNSUPPORTED             # forward-only head dims
-    assert bwd_call(d=192) == fa.FA_ERR_UNSUPPORTED
+    assert bwd_call(d=320) == fa.FA_ERR_UNSUPPORTED
+    assert bwd_call(d=160) == fa.FA_ERR_UNSUPPORTED
+    assert bwd_call(d=256, workspace_bytes=1024) == fa.FA_ERR_INVALID_ARG  # 256 is supported
     assert bwd_call(dk=FAKE + 4) == fa.FA_ERR_INVALID_ARG
     assert bwd_call(D=None) == fa.FA_ERR_INVALID_ARG
     assert bwd_call(workspace_bytes=1024) == fa.FA_ERR_INVALID_ARG
@@ -249,7 +251,7 @@ int main(void) {
     if (fa_fwd(p, p, p, p, FA_BF16, (float*)p, 2, 4, 3, 64, 0, 64, 0.125f, 1, NULL, p, 1 << 20,
                NULL) != FA_ERR_INVALID_ARG) return 3;
     if (fa_bwd(p, p, p, p, (const float*)p, (const float*)p, p, p, p, FA_BF16, p, 1 << 30, 2, 4,
-               2, 64, 0, 256, 0.1f, 0, NULL, 0, NULL) != FA_ERR_UNSUPPORTED) return 4;
+               2, 64, 0, 320, 0.1f, 0, NULL, 0, NULL) != FA_ERR_UNSUPPORTED) return 4;
     printf("%s\n", fa_version());
     return 0;
 }

@@ -232,12 +232,14 @@ def test_mid_dense_deterministic():
 
 
 @pytest.mark.parametrize("name", ["mid_causal_d192", "mid_causal_d256"])
-def test_wide_head_forward_full(name):
-    """Forward at head dimensions 192 and 256 on the benchmark's workload: 1024
+def test_wide_head_full(name):
+    """Head dimensions 192 and 256 on the benchmark's workload.  Forward: 1024
     one-tile units on 152 CTAs, so every CTA walks several units and the two
-    score buffers alternate across unit boundaries.  Whole heads and sampled
+    score buffers alternate across unit boundaries; whole heads and sampled
     rows against the oracle, in bf16 and fp32 O; repeats are bit-identical
-    (every unit writes only its own rows)."""
+    (every unit writes only its own rows).  Backward: whole heads, sampled
+    rows and keys, fp32 gradients against the literal bound, and the
+    deterministic mode bit-identical over repeats."""
     w = synth.workloads()[name]
     inp = synth.make_workload(w)
     x = cuda_inputs(inp)
@@ -267,3 +269,23 @@ def test_wide_head_forward_full(name):
             o2, lse2 = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale,
                                   batch=w.B, out_dtype=out_dtype)
             assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    # the backward (two passes per key/value tile, Q and dO by column chunks): whole
+    # heads and sampled keys in bf16, the literal bound in fp32, deterministic repeats
+    o, lse = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, batch=w.B)
+    for grad_dtype in (torch.bfloat16, torch.float32):
+        g = fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=w.causal,
+                        scale=w.scale, batch=w.B, grad_dtype=grad_dtype, check_status=True)
+        torch.cuda.synchronize()
+        got = dict(o=o, lse=lse, dq=g[0], dk=g[1], dv=g[2])
+        stored = grad_dtype == torch.bfloat16
+        if stored:
+            check_whole_head(w, inp, got, 0, 0)
+        check_rows(w, inp, got, [(2, 3)], rng, nrows=16, stored_bf16=stored)
+        check_keys(w, inp, got, [(1, 9)], rng, lo_frac=0.0, nkeys=8, stored_bf16=stored,
+                   first_keys=2)
+    det = [fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=w.causal, scale=w.scale,
+                       batch=w.B, deterministic=True, check_status=True) for _ in range(3)]
+    for a, b in zip(det[0], det[1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(det[0], det[2]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
