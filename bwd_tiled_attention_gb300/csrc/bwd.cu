@@ -968,32 +968,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // with per-row fp32 vector reductions, ordered by the same semaphores as the
 // main kernel in deterministic mode.
 constexpr int kWideThreads = 128;
-constexpr int kWideSlots = 4;    // ring of 64-column Q/dO chunks
-constexpr int kWideAhead = 2;    // chunks loaded ahead of the one an MMA reads
 constexpr int kWideChunkBytes = kTile * 64 * 2;
+// Ring of 64-column Q/dO chunks: 4 slots at d = 256 (all the shared memory
+// left), 6 at d = 192; loads are issued up to slots - 1 chunks ahead of the
+// MMA that reads them (the slot of chunk k + slots - 1 is the one chunk k - 1
+// read, whose MMA was issued before chunk k's).
+template <int D>
+struct WideCfg {
+    static constexpr int kSlots = D == 256 ? 4 : 6;
+    static constexpr int kAhead = kSlots - 1;
+};
 
 template <int D>
 struct WideSmem {
     alignas(1024) uint8_t k[kTile * D * 2];
     alignas(1024) uint8_t v[kTile * D * 2];
-    alignas(1024) uint8_t ring[kWideSlots][kWideChunkBytes];
-    alignas(1024) uint8_t ds[kTile * kTile * 2];  // dS^T, two 64-column boxes, 128B-swizzled
+    alignas(1024) uint8_t ring[WideCfg<D>::kSlots][kWideChunkBytes];
+    // dS^T (two 64-column boxes, 128B-swizzled); once dK and dQ have read it,
+    // the staging of the dQ merge (two 32-column fp32 slots)
+    alignas(1024) uint8_t ds[kTile * kTile * 2];
     alignas(16) float lse2[kTile];
     alignas(16) float dd[kTile];
     alignas(8) uint64_t kv_full, mma_done, drain;
-    uint64_t slot_full[kWideSlots], slot_free[kWideSlots];
+    uint64_t slot_full[WideCfg<D>::kSlots], slot_free[WideCfg<D>::kSlots];
     int2 unit;
     uint32_t tmem_base;
     int abort_flag;
     int zero;
 };
 static_assert(sizeof(WideSmem<256>) <= 232448, "wide backward shared memory exceeds 227 KB");
+static_assert(sizeof(WideSmem<192>) <= 232448, "wide backward shared memory exceeds 227 KB");
 
 template <int D, bool KV>
 __global__ void __launch_bounds__(kWideThreads, 1)
     fa_bwd_wide_kernel(const __grid_constant__ BwdParams p) {
     pdl_trigger();
     constexpr int C = D / 64;                       // 64-column chunks of a row
+    constexpr int kSlots = WideCfg<D>::kSlots;
     constexpr uint32_t kColDKV = 256;               // dV (pass 1), then dK (pass 2)
     constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
     constexpr uint32_t idN = make_idesc_bf16(128, 64, false, true);
@@ -1020,7 +1031,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         mbar_init(smem_u32(&sm.kv_full), 1);
         mbar_init(smem_u32(&sm.mma_done), 1);
         mbar_init(smem_u32(&sm.drain), 1);
-        for (int s = 0; s < kWideSlots; ++s) {
+        for (int s = 0; s < kSlots; ++s) {
             mbar_init(smem_u32(&sm.slot_full[s]), 1);
             mbar_init(smem_u32(&sm.slot_free[s]), 1);
         }
@@ -1083,17 +1094,17 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 hi = c < x.L ? min(kTile, x.L - i * kTile) : 0;
             }
         };
-        // LSE (base 2) and D of query tile i's rows into shared memory
-        auto load_rows = [&](int i) {
+        // LSE (base 2) and D of this thread's query row of tile i; the next
+        // step's are loaded while the current step runs
+        auto fetch_rows = [&](int i, float& l2, float& dv) {
             const int q = i * kTile + tid;
-            float l2 = 0.f, dv = 0.f;
+            l2 = 0.f;
+            dv = 0.f;
             if (q < x.L) {
                 const size_t at = (size_t)h * p.T + (size_t)(x.t0 + q);
                 l2 = p.lse[at] * kLog2e;
                 dv = p.D[at];
             }
-            sm.lse2[tid] = l2;
-            sm.dd[tid] = dv;
         };
 
         if (tid == 0) {
@@ -1119,7 +1130,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 kmax = min(kmax, total);
                 while (issued < kmax) {
                     const int k = issued, g = g0 + k;
-                    const int slot = g % kWideSlots, n = g / kWideSlots;
+                    const int slot = g % kSlots, n = g / kSlots;
                     if (n > 0 && !mbar_wait(smem_u32(&sm.slot_free[slot]), (n - 1) & 1, abort_flag)) {
                         raise_abort(abort_flag, hdr, kErrTimeout);
                         return false;
@@ -1138,24 +1149,28 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             };
             // thread 0: wait for chunk k (issuing loads ahead); returns its address or 0
             auto acquire = [&](int k) -> uint32_t {
-                if (!issue_upto(k + 1 + kWideAhead)) return 0u;
+                if (!issue_upto(k + 1 + WideCfg<D>::kAhead)) return 0u;
                 const int g = g0 + k;
-                if (!mbar_wait(smem_u32(&sm.slot_full[g % kWideSlots]), (g / kWideSlots) & 1,
+                if (!mbar_wait(smem_u32(&sm.slot_full[g % kSlots]), (g / kSlots) & 1,
                                abort_flag)) {
                     raise_abort(abort_flag, hdr, kErrTimeout);
                     return 0u;
                 }
                 tc_fence_after();
-                return smem_u32(sm.ring[g % kWideSlots]);
+                return smem_u32(sm.ring[g % kSlots]);
             };
             auto release = [&](int k) {
-                mma_commit(smem_u32(&sm.slot_free[(g0 + k) % kWideSlots]));
+                mma_commit(smem_u32(&sm.slot_free[(g0 + k) % kSlots]));
             };
 
+            float nl2 = 0.f, ndd = 0.f;
+            if (x.ns > 0) fetch_rows(walk_tile<KV>(x, 0, p.deterministic, p.causal), nl2, ndd);
             for (int s = 0; s < x.ns; ++s) {
                 const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
-                load_rows(i);
+                sm.lse2[tid] = nl2;  // (the previous step's readers are past a block barrier)
+                sm.dd[tid] = ndd;
                 __syncthreads();
+                if (s + 1 < x.ns) fetch_rows(walk_tile<KV>(x, s + 1, p.deterministic, p.causal), nl2, ndd);
                 // S^T = K Q_i^T into [0, 128); pass 2 also dP^T = V dO_i^T into [128, 256)
                 if (tid == 0) {
                     for (int cc = 0; cc < C; ++cc) {
@@ -1285,19 +1300,59 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         raise_abort(abort_flag, hdr, kErrTimeout);
                 }
                 if (__syncthreads_or(*abort_flag != 0)) { ok = false; break; }
-                const int qr = i * kTile + tid;
-                float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + h) * D;
+                const int row0 = i * kTile;
+                const int qr = row0 + tid;
+                if (row0 + kTile <= x.L) {
+                    // whole tile: bulk tensor reduce-adds of 32 columns, staged
+                    // 128B-swizzled through the dS buffer (dK and dQ have read it)
+                    const uint32_t stage_base = dsaddr;
+                    uint8_t* stage_row = sm.ds + tid * 128;
+                    const int sw = tid & 7;
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + cc * 32, v);
-                    tmem_ld_wait();
-                    if (qr < x.L) {
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        const int sl = cc & 1;
+                        uint32_t v[32];
+                        tmem_ld32(tmem + lane_off + cc * 32, v);
+                        tmem_ld_wait();
+                        if (tid == 0 && cc >= 2) bulk_wait_group_read<1>();  // the slot's last reduce read it
+                        __syncthreads();
+                        uint8_t* row = stage_row + sl * (kTile * 128);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[4 * e]),
-                                       __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
-                                       __uint_as_float(v[4 * e + 3]));
+                            *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) =
+                                make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                        fence_proxy_async_smem();
+                        __syncthreads();
+                        if (tid == 0) {
+                            tma_reduce_add_3d(&p.tm_dq_acc, stage_base + sl * (kTile * 128), cc * 32,
+                                              h, x.t0 + row0);
+                            bulk_commit_group();
+                        }
+                    }
+                    // the next step writes dS^T over the staging: its reduces must have read it
+                    if (tid == 0) {
+                        if (p.deterministic) {
+                            bulk_wait_group<0>();
+                            fence_proxy_async_global();
+                        } else {
+                            bulk_wait_group_read<0>();
+                        }
+                    }
+                } else {
+                    // ragged last tile of a sequence: per-row vector reductions
+                    float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + h) * D;
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + lane_off + cc * 32, v);
+                        tmem_ld_wait();
+                        if (qr < x.L) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[4 * e]),
+                                           __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
+                                           __uint_as_float(v[4 * e + 3]));
+                        }
                     }
                 }
                 tc_fence_before();
@@ -1370,11 +1425,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (tid == 0) {
         const volatile int* z = &sm.zero;
         const int last = g0 + issued;  // chunks whose loads were issued
-        for (int e = 0; e < kWideSlots && e < last; ++e) {
+        for (int e = 0; e < kSlots && e < last; ++e) {
             const int g = last - 1 - e;
-            mbar_wait(smem_u32(&sm.slot_full[g % kWideSlots]), (g / kWideSlots) & 1, z);
+            mbar_wait(smem_u32(&sm.slot_full[g % kSlots]), (g / kSlots) & 1, z);
         }
         if (kv_issued > 0) mbar_wait(smem_u32(&sm.kv_full), (kv_issued - 1) & 1, z);
+        bulk_wait_group<0>();  // no reduce may still read the staging
         mma_commit(smem_u32(&sm.drain));
         mbar_wait(smem_u32(&sm.drain), 0, z);
     }

@@ -3,10 +3,11 @@ timings (CPU).
 
 Above d = 128 one thread issues every TMA load and MMA of the backward, and
 the 128 threads of the block meet at block barriers between the phases, so
-the only pipelined hand-off is the ring of 64-column Q/dO chunks: the issuer
-loads a chunk into slot g % 4 once the MMA that read the slot's previous chunk
-has completed (slot_free, phase g / 4 - 1), and an MMA reads chunk g once its
-load has landed (slot_full, phase g / 4), with loads issued up to two chunks
+the only pipelined hand-off is the ring of 64-column Q/dO chunks (4 slots at
+d = 256, 6 at d = 192): the issuer loads a chunk into slot g % slots once the
+MMA that read the slot's previous chunk has completed (slot_free, phase
+g / slots - 1), and an MMA reads chunk g once its load has landed
+(slot_full, phase g / slots), with loads issued up to slots - 1 chunks
 ahead of the MMA that needs them, within the pass.  Pass 1 of a unit reads
 per query tile Q then dO (C chunks each), pass 2 Q, dO, then Q again; the
 ring's position carries over from pass to pass and unit to unit.
@@ -21,7 +22,6 @@ import random
 
 import pytest
 
-SLOTS = 4
 
 
 class Hazard(Exception):
@@ -39,8 +39,9 @@ class Bar:
         return (self.phases & 1) != parity
 
 
-def run(units, C, seed, ahead=2, mistake=None):
+def run(units, C, seed, slots, ahead, mistake=None):
     """units: list of step counts (query tiles per unit, 0 allowed)."""
+    SLOTS = slots
     rnd = random.Random(seed)
     full = [Bar() for _ in range(SLOTS)]
     free = [Bar() for _ in range(SLOTS)]
@@ -153,25 +154,30 @@ def random_units(rnd):
     return [rnd.choice([0, 1, 2, 3, 5]) for _ in range(rnd.randint(1, 5))]
 
 
-@pytest.mark.parametrize("C", [3, 4])
-def test_ring_is_hazard_and_deadlock_free(C):
+# (chunks per row, ring slots): d = 192 and d = 256
+RINGS = [(3, 6), (4, 4)]
+
+
+@pytest.mark.parametrize("C,slots", RINGS)
+def test_ring_is_hazard_and_deadlock_free(C, slots):
     for seed in range(300):
         units = random_units(random.Random(seed))
-        n = run(units, C, seed)
+        n = run(units, C, seed, slots, slots - 1)
         assert n == sum(ns * 5 * C for ns in units)  # 2C + 3C chunks per step, one MMA each
 
 
 # Each planted mistake must be caught:
 # - no_slot_free_wait: a load may land over a chunk an MMA has yet to read;
 # - wrong_free_phase: waiting for the wrong completion of slot_free;
-# - too_far_ahead: five chunks in flight on four slots.
+# - too_far_ahead: loads issued as many chunks ahead as there are slots.
+@pytest.mark.parametrize("C,slots", RINGS)
 @pytest.mark.parametrize("mistake", ["no_slot_free_wait", "wrong_free_phase", "too_far_ahead"])
-def test_ring_planted_mistakes(mistake):
+def test_ring_planted_mistakes(mistake, C, slots):
     caught = False
     for seed in range(300):
         units = random_units(random.Random(seed))
         try:
-            run(units, 4, seed, ahead=4 if mistake == "too_far_ahead" else 2,
+            run(units, C, seed, slots, slots if mistake == "too_far_ahead" else slots - 1,
                 mistake=None if mistake == "too_far_ahead" else mistake)
         except Hazard:
             caught = True
