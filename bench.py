@@ -47,19 +47,50 @@ METRIC_FWD = "attention fwd BF16 TFLOPs/s and % of GB300 dense BF16 peak"
 # kernels and their schedule at the time of the capture.  When the sources
 # have changed since, the figure no longer describes the kernels and the
 # bench reports null.
-FA_BWD_DRAM = {"mid_causal": {"bytes": 774.1e6, "sources": "52dc384806971988"}}
+FA_BWD_DRAM = {"mid_causal": {"bytes": 775.9e6, "sources": "9568809f82eed151"}}
 TRAFFIC_SOURCES = ["bwd_tiled_attention_gb300/csrc/" + f
                    for f in ("bwd.cu", "sched.cu", "api.cu", "common.cuh", "sm100_ptx.cuh",
                              "internal.h")]
 NOMINAL_PEAK_TFLOPS = 2250.0
 
 
+def code_tokens(text):
+    """C/C++/CUDA source with its comments removed and every run of whitespace
+    made one space: a change to a comment or to the layout leaves it as is,
+    a change to the code does not.  String and character literals are kept
+    whole (a "//" inside one is not a comment)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and text[j] != ch:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def sources_sha(files=TRAFFIC_SOURCES):
+    """sha256 (first 16 hex digits) of the code of the backward's sources,
+    comments and layout excluded."""
     import hashlib
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(code_tokens(fh.read()).encode())
+            h.update(b"\0")
     return h.hexdigest()[:16]
 
 
@@ -417,8 +448,12 @@ def rates(r, t):
 
 
 # The other configurations of the tiled-attention workloads, each timed the way
-# the headline is (L2 flushed before every step, CUDA events, >= 1 s of steps).
-PER_CONFIG = ["tiny", "mid_dense", "long_causal", "gqa8_causal", "mqa_causal", "varlen_det"]
+# the headline is (L2 flushed before every step, CUDA events, >= 1 s of steps):
+# the small, dense, long, grouped and packed deterministic ones, then other
+# head dimensions and queries shorter than keys.
+PER_CONFIG = ["tiny", "mid_dense", "long_causal", "gqa8_causal", "mqa_causal", "varlen_det",
+              "mid_causal_d64", "mid_causal_d96", "mid_causal_d192", "mid_causal_d256",
+              "chunk_causal"]
 
 
 def per_config(fa, dev, flush, local, names=PER_CONFIG, target_s=1.0):

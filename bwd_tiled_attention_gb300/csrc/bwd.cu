@@ -959,14 +959,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //           dK += dS^T Q, dQ = dS K into the columns S^T and dP^T held.
 // dV is stored after pass 1 and dK after pass 2, from the same TMEM columns
 // [256, 256 + d).  K and V stay in shared memory for the unit; Q and dO are
-// streamed in 64-column chunks through a 4-slot ring, loaded two chunks ahead
-// of the MMA that reads them (pass 1 reads Q, dO; pass 2 reads Q, dO, Q), so
-// pass 2 recomputes S and the MMA work is 1.2 times the five products.  One
-// thread issues every load and MMA; all 128 threads (one per key row, or one
-// per query row in the dQ merge) do the elementwise work between them, and
-// every hand-off is a bounded mbarrier wait or a block barrier.  dQ is merged
-// with per-row fp32 vector reductions, ordered by the same semaphores as the
-// main kernel in deterministic mode.
+// streamed in 64-column chunks through a ring (pass 1 reads Q, dO; pass 2
+// reads Q, dO, Q), so pass 2 recomputes S and the MMA work is 1.2 times the
+// five products.  One thread issues every load and MMA; all 128 threads (one
+// per key row, or one per query row in the dQ merge) do the elementwise work
+// between them, and every hand-off is a bounded mbarrier wait or a block
+// barrier.  dQ is merged with bulk tensor reduce-adds of 32-column fp32
+// slices staged through the dS buffer (per-row vector reductions on a ragged
+// last tile), ordered by the same semaphores as the main kernel in
+// deterministic mode.
 constexpr int kWideThreads = 128;
 constexpr int kWideChunkBytes = kTile * 64 * 2;
 // Ring of 64-column Q/dO chunks: 4 slots at d = 256 (all the shared memory

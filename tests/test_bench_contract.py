@@ -70,3 +70,23 @@ def test_steps_for_fills_the_clock_window():
     # a 0.34 ms step plus the flush: about 2 s of steps
     assert 4000 <= bench.steps_for(0.34, 2.0, lo=200) <= 5000
     assert bench.steps_for(100.0, 1.0, lo=10) == 10
+
+
+def test_traffic_hash_ignores_comments_not_code(tmp_path):
+    """A comment or layout edit keeps the recorded traffic; a code edit drops it."""
+    import bench
+    src = 'int f(int a) {  // one\n  /* two */ return a + 1; }\nconst char* s = "x//y";\n'
+    variants = {
+        "base": src,
+        "comment": src.replace("// one", "// another comment").replace("/* two */", ""),
+        "layout": src.replace("  return", "\n\n        return"),
+        "code": src.replace("a + 1", "a + 2"),
+        "string": src.replace("x//y", "x//z"),
+    }
+    sha = {}
+    for k, text in variants.items():
+        f = tmp_path / f"{k}.cu"
+        f.write_text(text)
+        sha[k] = bench.sources_sha([str(f)])
+    assert sha["comment"] == sha["base"] and sha["layout"] == sha["base"]
+    assert sha["code"] != sha["base"] and sha["string"] != sha["base"]
