@@ -961,23 +961,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // [256, 256 + d).  K and V stay in shared memory for the unit; Q and dO are
 // streamed in 64-column chunks through a ring (pass 1 reads Q, dO; pass 2
 // reads Q, dO, Q), so pass 2 recomputes S and the MMA work is 1.2 times the
-// five products.  One thread issues every load and MMA; all 128 threads (one
-// per key row, or one per query row in the dQ merge) do the elementwise work
-// between them, and every hand-off is a bounded mbarrier wait or a block
-// barrier.  dQ is merged with bulk tensor reduce-adds of 32-column fp32
-// slices staged through the dS buffer (per-row vector reductions on a ragged
-// last tile), ordered by the same semaphores as the main kernel in
-// deterministic mode.
-constexpr int kWideThreads = 128;
+// five products.
+//
+// A step streams 128 KB (pass 1) or 192 KB (pass 2) of chunks, and a TMA load
+// blocks its issuing thread while the SM's TMA unit works through the loads
+// before it (about 25 B per cycle per SM), so the loads have a warp of their
+// own, as do the MMAs.  Roles (256 threads):
+//   warp 0       producer: unit fetch, K and V, the Q/dO chunks in the order
+//                the MMAs read them
+//   warp 1       MMA issuer (one thread)
+//   warp 2       TMEM allocation
+//   warps 4..7   compute, one thread per key row (P^T, dS^T, the dK/dV
+//                epilogue) or per query row (the dQ merge)
+// Pass 1 double-buffers S^T in TMEM columns [0, 128) and [128, 256): the MMA
+// issuer computes S^T of the next query tile while the compute warps turn the
+// current one into P^T, then dV.  Pass 2 computes S^T and dP^T, waits for dS^T,
+// then dK and dQ; the compute warps release dQ's columns in two halves as the
+// merge reads them, so the next S^T starts while the merge still runs.
+constexpr int kWideThreads = 256;
 constexpr int kWideChunkBytes = kTile * 64 * 2;
 // Ring of 64-column Q/dO chunks: 4 slots at d = 256 (all the shared memory
-// left), 6 at d = 192; loads are issued up to slots - 1 chunks ahead of the
-// MMA that reads them (the slot of chunk k + slots - 1 is the one chunk k - 1
-// read, whose MMA was issued before chunk k's).
+// left), 6 at d = 192.
 template <int D>
 struct WideCfg {
     static constexpr int kSlots = D == 256 ? 4 : 6;
-    static constexpr int kAhead = kSlots - 1;
 };
 
 template <int D>
@@ -988,17 +995,31 @@ struct WideSmem {
     // dS^T (two 64-column boxes, 128B-swizzled); once dK and dQ have read it,
     // the staging of the dQ merge (two 32-column fp32 slots)
     alignas(1024) uint8_t ds[kTile * kTile * 2];
-    alignas(16) float lse2[kTile];
-    alignas(16) float dd[kTile];
-    alignas(8) uint64_t kv_full, mma_done, drain;
+    alignas(16) float lse2[2][kTile];  // LSE * log2(e) of the step's query rows
+    alignas(16) float dd[2][kTile];    // D of the step's query rows
+    alignas(8) uint64_t sched_full[2], sched_empty[2];
+    uint64_t kv_full, kv_empty;
     uint64_t slot_full[WideCfg<D>::kSlots], slot_free[WideCfg<D>::kSlots];
-    int2 unit;
+    uint64_t s_full[2], p_ready[2], s_free[2];            // pass 1, per S^T buffer
+    uint64_t sdp_full, ds_ready, dq_full, dq_free[2];     // pass 2; dQ columns in halves
+    uint64_t dv_full, dk_full;                            // dV / dK done
+    uint64_t drain;
+    int2 sched[2];
     uint32_t tmem_base;
     int abort_flag;
     int zero;
 };
 static_assert(sizeof(WideSmem<256>) <= 232448, "wide backward shared memory exceeds 227 KB");
 static_assert(sizeof(WideSmem<192>) <= 232448, "wide backward shared memory exceeds 227 KB");
+
+// One write-after-read hand-off of a TMEM region that the MMA issuer still
+// has to wait for: the barrier and the parity of the phase.  The issuer waits
+// for it before its next write to the region, and before recording another
+// one for the same region, so it is never two phases behind a barrier.
+struct Pending {
+    uint32_t bar = 0, parity = 0;
+    bool set = false;
+};
 
 template <int D, bool KV>
 __global__ void __launch_bounds__(kWideThreads, 1)
@@ -1025,22 +1046,35 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + p.dq_acc_off);
     float* dk_acc = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + p.dk_acc_off);
     float* dv_acc = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + p.dv_acc_off);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int warp = warp_id(), lane = lane_id();
     volatile int* abort_flag = &sm.abort_flag;
 
-    if (tid == 0) {
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&sm.sched_full[i]), 1);
+            mbar_init(smem_u32(&sm.sched_empty[i]), 1 + 4);
+            mbar_init(smem_u32(&sm.s_full[i]), 1);
+            mbar_init(smem_u32(&sm.p_ready[i]), 4);
+            mbar_init(smem_u32(&sm.s_free[i]), 1);
+            mbar_init(smem_u32(&sm.dq_free[i]), 4);
+        }
         mbar_init(smem_u32(&sm.kv_full), 1);
-        mbar_init(smem_u32(&sm.mma_done), 1);
-        mbar_init(smem_u32(&sm.drain), 1);
+        mbar_init(smem_u32(&sm.kv_empty), 1);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(smem_u32(&sm.slot_full[s]), 1);
             mbar_init(smem_u32(&sm.slot_free[s]), 1);
         }
+        mbar_init(smem_u32(&sm.sdp_full), 1);
+        mbar_init(smem_u32(&sm.ds_ready), 4);
+        mbar_init(smem_u32(&sm.dq_full), 1);
+        mbar_init(smem_u32(&sm.dv_full), 1);
+        mbar_init(smem_u32(&sm.dk_full), 1);
+        mbar_init(smem_u32(&sm.drain), 1);
         sm.abort_flag = 0;
         sm.zero = 0;
         fence_barrier_init();
     }
-    if (warp == 0) {
+    if (warp == 2) {
         tmem_alloc(smem_u32(&sm.tmem_base), 512);
         tmem_relinquish();
     }
@@ -1051,393 +1085,493 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     pdl_wait();  // the unit list, LSE, D and the reset workspace are the previous kernels' output
     const int n_units = hdr->n_units;
     const int n_qtiles = hdr->n_qtiles;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t kaddr = smem_u32(sm.k), vaddr = smem_u32(sm.v), dsaddr = smem_u32(sm.ds);
-    const uint32_t mbar_mma = smem_u32(&sm.mma_done);
 
-    // Ring state (thread 0): chunks consumed before the current pass, and the
-    // pass's chunks whose loads were issued.
-    int g0 = 0, issued = 0;
-    int mma_waits = 0, kv_waits = 0;  // phases of mma_done / kv_full waited for
-    int kv_issued = 0;                // (thread 0) K/V loads issued
-    // ok changes only right after a block-wide vote (__syncthreads_or), so every
-    // thread takes the same branches around the block barriers.
-    bool ok = true;
-
-    // Every thread waits for the next phase of mma_done.
-    auto wait_mma = [&]() {
-        if (!mbar_wait(mbar_mma, mma_waits & 1, abort_flag)) raise_abort(abort_flag, hdr, kErrTimeout);
-        ++mma_waits;
-        tc_fence_after();
-    };
-
-    while (true) {
-        if (tid == 0) {
-            const int u = atomicAdd(&hdr->counter, 1);
-            sm.unit = u < n_units ? units[u] : make_int2(-1, 0);
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            tma_prefetch_desc(&p.tm_do);
+            int sched_it = 0, unit_it = 0, g = 0;  // g: chunks loaded, over all units
+            bool ok = true;
+            // chunk of query tile i: Q or dO columns [64 cc, +64)
+            auto load_chunk = [&](bool is_do, int cc, int h, int row0) -> bool {
+                const int slot = g % kSlots, n = g / kSlots;
+                if (n > 0 && !wait_or_abort(smem_u32(&sm.slot_free[slot]), (n - 1) & 1, abort_flag, hdr))
+                    return false;
+                const uint32_t bar = smem_u32(&sm.slot_full[slot]);
+                mbar_arrive_expect_tx(bar, kWideChunkBytes);
+                tma_load_3d(smem_u32(sm.ring[slot]), is_do ? &p.tm_do : &p.tm_q, bar, cc * 64, h, row0);
+                ++g;
+                return true;
+            };
+            while (ok) {
+                const int slot = sched_it & 1;
+                if (!(ok = wait_or_abort(smem_u32(&sm.sched_empty[slot]), ((sched_it >> 1) & 1) ^ 1,
+                                         abort_flag, hdr)))
+                    break;
+                const int u = atomicAdd(&hdr->counter, 1);
+                const int2 unit = u < n_units ? units[u] : make_int2(-1, 0);
+                sm.sched[slot] = unit;
+                mbar_arrive(smem_u32(&sm.sched_full[slot]));
+                ++sched_it;
+                if (unit.x < 0) break;
+                const BUnit x = decode_bunit<KV, false>(unit, p);
+                const int h = x.h0;
+                if (unit_it > 0 &&
+                    !(ok = wait_or_abort(smem_u32(&sm.kv_empty), (unit_it - 1) & 1, abort_flag, hdr)))
+                    break;
+                const uint32_t kvbar = smem_u32(&sm.kv_full);
+                mbar_arrive_expect_tx(kvbar, 2 * kTile * D * 2);
+                for (int cb = 0; cb < C; ++cb) {
+                    tma_load_3d(kaddr + cb * 16384, &p.tm_k, kvbar, cb * 64, x.g, x.tk0 + x.j * kTile);
+                    tma_load_3d(vaddr + cb * 16384, &p.tm_v, kvbar, cb * 64, x.g, x.tk0 + x.j * kTile);
+                }
+                ++unit_it;
+                auto row0 = [&](int s) {
+                    return x.t0 + walk_tile<KV>(x, s, p.deterministic, p.causal) * kTile;
+                };
+                // pass 1: Q(0), then Q(s), dO(s - 1) for s >= 1, then dO(n - 1)
+                for (int s = 0; s <= x.ns && ok; ++s) {
+                    for (int cc = 0; cc < C && ok && s < x.ns; ++cc) ok = load_chunk(false, cc, h, row0(s));
+                    for (int cc = 0; cc < C && ok && s > 0; ++cc) ok = load_chunk(true, cc, h, row0(s - 1));
+                }
+                // pass 2: Q(s), dO(s), Q(s)
+                for (int s = 0; s < x.ns && ok; ++s) {
+                    const int r0 = row0(s);
+                    for (int cc = 0; cc < C && ok; ++cc) ok = load_chunk(false, cc, h, r0);
+                    for (int cc = 0; cc < C && ok; ++cc) ok = load_chunk(true, cc, h, r0);
+                    for (int cc = 0; cc < C && ok; ++cc) ok = load_chunk(false, cc, h, r0);
+                }
+            }
+            // never leave a TMA write in flight
+            const volatile int* z = &sm.zero;
+            for (int e = 0; e < kSlots && e < g; ++e) {
+                const int it = g - 1 - e;
+                mbar_wait(smem_u32(&sm.slot_full[it % kSlots]), (it / kSlots) & 1, z);
+            }
+            if (unit_it > 0) mbar_wait(smem_u32(&sm.kv_full), (unit_it - 1) & 1, z);
         }
-        __syncthreads();
-        const int2 unit = sm.unit;
-        if (__syncthreads_or(unit.x < 0 || *abort_flag != 0)) break;
-        const BUnit x = decode_bunit<KV, false>(unit, p);
-        const int h = x.h0;
-        // this thread's key row (P, dS phases; dK/dV epilogue): key position c
-        // within its sequence; query column r of tile i sees it iff it is in [lo, hi)
-        const int c = x.j * kTile + tid;
-        const int c_off = c - x.off;
-        const int L_vis = c < x.Lk ? x.L : 0;
-        auto visible = [&](int i, int& lo, int& hi) {
-            if constexpr (KV) {
-                lo = p.causal ? max(0, c_off - i * kTile) : 0;
-                hi = min(kTile, L_vis - i * kTile);
-            } else {
-                lo = p.causal ? max(0, c - i * kTile) : 0;
-                hi = c < x.L ? min(kTile, x.L - i * kTile) : 0;
-            }
-        };
-        // LSE (base 2) and D of this thread's query row of tile i; the next
-        // step's are loaded while the current step runs
-        auto fetch_rows = [&](int i, float& l2, float& dv) {
-            const int q = i * kTile + tid;
-            l2 = 0.f;
-            dv = 0.f;
-            if (q < x.L) {
-                const size_t at = (size_t)h * p.T + (size_t)(x.t0 + q);
-                l2 = p.lse[at] * kLog2e;
-                dv = p.D[at];
-            }
-        };
-
-        if (tid == 0) {
-            const uint32_t bar = smem_u32(&sm.kv_full);
-            mbar_arrive_expect_tx(bar, 2 * kTile * D * 2);
-            for (int cb = 0; cb < C; ++cb) {
-                tma_load_3d(kaddr + cb * 16384, &p.tm_k, bar, cb * 64, x.g, x.tk0 + x.j * kTile);
-                tma_load_3d(vaddr + cb * 16384, &p.tm_v, bar, cb * 64, x.g, x.tk0 + x.j * kTile);
-            }
-            ++kv_issued;
-        }
-        if (!mbar_wait(smem_u32(&sm.kv_full), kv_waits & 1, abort_flag))
-            raise_abort(abort_flag, hdr, kErrTimeout);
-        ++kv_waits;
-        if (__syncthreads_or(*abort_flag != 0)) break;
-
-        for (int pass = 0; pass < 2 && ok; ++pass) {
-            const int per = pass == 0 ? 2 * C : 3 * C;  // chunks read per step
-            const int total = x.ns * per;
-            // chunk k of the pass: query tile of step k / per; Q columns, then dO
-            // columns, then (pass 2) Q columns again
-            auto issue_upto = [&](int kmax) -> bool {
-                kmax = min(kmax, total);
-                while (issued < kmax) {
-                    const int k = issued, g = g0 + k;
-                    const int slot = g % kSlots, n = g / kSlots;
-                    if (n > 0 && !mbar_wait(smem_u32(&sm.slot_free[slot]), (n - 1) & 1, abort_flag)) {
-                        raise_abort(abort_flag, hdr, kErrTimeout);
-                        return false;
-                    }
-                    const int s = k / per, w = k - s * per;
-                    const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
-                    const bool is_do = w >= C && w < 2 * C;
-                    const int col = (w % C) * 64;
-                    const uint32_t bar = smem_u32(&sm.slot_full[slot]);
-                    mbar_arrive_expect_tx(bar, kWideChunkBytes);
-                    tma_load_3d(smem_u32(sm.ring[slot]), is_do ? &p.tm_do : &p.tm_q, bar, col, h,
-                                x.t0 + i * kTile);
-                    ++issued;
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int sched_it = 0, unit_it = 0, g = 0;  // g: chunks consumed, over all units
+            int c1 = 0, c2 = 0;                    // pass-1 / pass-2 steps, over all units
+            // TMEM [0, 128) and [128, 256).  The dK/dV columns need none: the
+            // compute warps read dV out before they arrive on ds_ready (pass 2's
+            // first dK waits for it) and dK before the next unit's first p_ready.
+            Pending pend_s[2];
+            bool ok = true;
+            auto settle = [&](Pending& pd) -> bool {
+                if (!pd.set) return true;
+                pd.set = false;
+                if (!wait_or_abort(pd.bar, pd.parity, abort_flag, hdr)) return false;
+                tc_fence_after();
+                return true;
+            };
+            auto expect = [&](Pending& pd, uint32_t bar, uint32_t parity) -> bool {
+                const bool r = settle(pd);
+                pd.bar = bar;
+                pd.parity = parity;
+                pd.set = true;
+                return r;
+            };
+            // next chunk of the ring: its shared-memory address once landed, or 0
+            auto acquire = [&]() -> uint32_t {
+                const int slot = g % kSlots;
+                if (!wait_or_abort(smem_u32(&sm.slot_full[slot]), (g / kSlots) & 1, abort_flag, hdr))
+                    return 0u;
+                tc_fence_after();
+                return smem_u32(sm.ring[slot]);
+            };
+            auto release = [&]() { mma_commit(smem_u32(&sm.slot_free[g++ % kSlots])); };
+            // S^T = K Q^T over C chunks into TMEM column col (accumulating across chunks)
+            auto issue_s = [&](uint32_t col, uint32_t abase) -> bool {
+                for (int cc = 0; cc < C; ++cc) {
+                    const uint32_t a = acquire();
+                    if (!a) return false;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tmem + col, make_sdesc(abase + cc * 16384 + kk * 32, 16, 1024),
+                               make_sdesc(a + kk * 32, 16, 1024), idS, (cc | kk) > 0);
+                    release();
                 }
                 return true;
             };
-            // thread 0: wait for chunk k (issuing loads ahead); returns its address or 0
-            auto acquire = [&](int k) -> uint32_t {
-                if (!issue_upto(k + 1 + WideCfg<D>::kAhead)) return 0u;
-                const int g = g0 + k;
-                if (!mbar_wait(smem_u32(&sm.slot_full[g % kSlots]), (g / kSlots) & 1,
-                               abort_flag)) {
-                    raise_abort(abort_flag, hdr, kErrTimeout);
-                    return 0u;
-                }
+            while (ok) {
+                const int slot = sched_it & 1;
+                if (!(ok = wait_or_abort(smem_u32(&sm.sched_full[slot]), (sched_it >> 1) & 1,
+                                         abort_flag, hdr)))
+                    break;
+                const int2 unit = sm.sched[slot];
+                mbar_arrive(smem_u32(&sm.sched_empty[slot]));
+                ++sched_it;
+                if (unit.x < 0) break;
+                const BUnit x = decode_bunit<KV, false>(unit, p);
+                if (!(ok = wait_or_abort(smem_u32(&sm.kv_full), unit_it & 1, abort_flag, hdr))) break;
                 tc_fence_after();
-                return smem_u32(sm.ring[g % kSlots]);
-            };
-            auto release = [&](int k) {
-                mma_commit(smem_u32(&sm.slot_free[(g0 + k) % kSlots]));
-            };
-
-            float nl2 = 0.f, ndd = 0.f;
-            if (x.ns > 0) fetch_rows(walk_tile<KV>(x, 0, p.deterministic, p.causal), nl2, ndd);
-            for (int s = 0; s < x.ns; ++s) {
-                const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
-                sm.lse2[tid] = nl2;  // (the previous step's readers are past a block barrier)
-                sm.dd[tid] = ndd;
-                __syncthreads();
-                if (s + 1 < x.ns) fetch_rows(walk_tile<KV>(x, s + 1, p.deterministic, p.causal), nl2, ndd);
-                // S^T = K Q_i^T into [0, 128); pass 2 also dP^T = V dO_i^T into [128, 256)
-                if (tid == 0) {
-                    for (int cc = 0; cc < C; ++cc) {
-                        const uint32_t a = acquire(s * per + cc);
-                        if (!a) break;  // (abort flag raised: every thread stops below)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tmem, make_sdesc(kaddr + cc * 16384 + kk * 32, 16, 1024),
-                                   make_sdesc(a + kk * 32, 16, 1024), idS, (cc | kk) > 0);
-                        release(s * per + cc);
+                ++unit_it;
+                // ---- pass 1: S(0), then S(s), dV(s - 1), then dV(n - 1)
+                for (int s = 0; s <= x.ns && ok; ++s) {
+                    if (s < x.ns) {
+                        const int c = c1 + s, b = c & 1;
+                        if (!(ok = settle(pend_s[b]))) break;
+                        if (!(ok = issue_s((uint32_t)b * 128, kaddr))) break;
+                        mma_commit(smem_u32(&sm.s_full[b]));
                     }
-                    for (int cc = 0; pass == 1 && cc < C; ++cc) {
-                        const uint32_t a = acquire(s * per + C + cc);
-                        if (!a) break;  // (abort flag raised: every thread stops below)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tmem + 128, make_sdesc(vaddr + cc * 16384 + kk * 32, 16, 1024),
-                                   make_sdesc(a + kk * 32, 16, 1024), idS, (cc | kk) > 0);
-                        release(s * per + C + cc);
-                    }
-                    mma_commit(mbar_mma);
-                }
-                wait_mma();
-                int lo, hi;
-                visible(i, lo, hi);
-                const bool full = lo == 0 && hi == kTile;
-                if (pass == 0) {
-                    // P^T of this key row, bf16, packed over the first 32 columns of
-                    // each 64-column half of S^T (query columns [64h + 16m, +16) in
-                    // TMEM columns [64h + 8m, +8)): the A operand of dV
-                    uint32_t sv[4][32];
-#pragma unroll
-                    for (int qc = 0; qc < 4; ++qc) tmem_ld32(tmem + lane_off + qc * 32, sv[qc]);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int qc = 0; qc < 4; ++qc) {
-                        uint32_t pk[16];
-                        if (full)
-                            p_chunk<false>(sv[qc], sm.lse2 + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
-                        else
-                            p_chunk<true>(sv[qc], sm.lse2 + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
-                        tmem_st16(tmem + lane_off + (qc >> 1) * 64 + (qc & 1) * 16, pk);
-                    }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    if (__syncthreads_or(*abort_flag != 0)) { ok = false; break; }
-                    // dV += P^T dO_i, 64 columns of dO per chunk
-                    if (tid == 0) {
+                    if (s > 0) {
+                        const int c = c1 + s - 1, b = c & 1;
+                        if (!(ok = wait_or_abort(smem_u32(&sm.p_ready[b]), (c >> 1) & 1, abort_flag, hdr)))
+                            break;
                         tc_fence_after();
-                        for (int cc = 0; cc < C; ++cc) {
-                            const uint32_t a = acquire(s * per + C + cc);
-                            if (!a) break;  // (abort flag raised: every thread stops below)
+                        for (int cc = 0; cc < C && ok; ++cc) {
+                            const uint32_t a = acquire();
+                            if (!(ok = a != 0)) break;
 #pragma unroll
                             for (int kk = 0; kk < kTile / 16; ++kk)
-                                mma_ts(tmem + kColDKV + cc * 64, tmem + (kk >> 2) * 64 + (kk & 3) * 8,
+                                mma_ts(tmem + kColDKV + cc * 64,
+                                       tmem + b * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
                                        make_sdesc(a + kk * 2048, 16384, 1024), idN,
-                                       (s > 0 || kk > 0) ? 1u : 0u);
-                            release(s * per + C + cc);
+                                       (s > 1 || kk > 0) ? 1u : 0u);
+                            release();
                         }
-                        mma_commit(mbar_mma);
-                    }
-                    wait_mma();  // dV read P^T: the next S may overwrite it
-                    if (__syncthreads_or(*abort_flag != 0)) { ok = false; break; }
-                    continue;
-                }
-                // pass 2: dS^T = P^T (dP^T - D), bf16, swizzled rows of the dS^T tile
-                uint8_t* ds_row = sm.ds + tid * 128;
-                const int sw = tid & 7;
-#pragma unroll 1
-                for (int qc = 0; qc < 4; ++qc) {
-                    uint32_t sv[32], dv[32];
-                    tmem_ld32(tmem + lane_off + qc * 32, sv);
-                    tmem_ld32(tmem + lane_off + 128 + qc * 32, dv);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
-                    if (full)
-                        p_chunk<false>(sv, sm.lse2 + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
-                    else
-                        p_chunk<true>(sv, sm.lse2 + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
-                    uint32_t out[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 pf =
-                            __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[e]));
-                        const float d0 = sm.dd[qc * 32 + 2 * e], d1 = sm.dd[qc * 32 + 2 * e + 1];
-                        out[e] = pack_bf16x2(pf.x * (__uint_as_float(dv[2 * e]) - d0),
-                                             pf.y * (__uint_as_float(dv[2 * e + 1]) - d1));
-                    }
-                    // 32 query columns = 4 chunks of 16 bytes of half (qc >> 1)'s block
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int ch = (qc & 1) * 4 + e;
-                        *reinterpret_cast<uint4*>(ds_row + (qc >> 1) * 16384 + ((ch ^ sw) << 4)) =
-                            make_uint4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]);
+                        if (!ok) break;
+                        mma_commit(smem_u32(&sm.s_free[b]));
+                        ok = expect(pend_s[b], smem_u32(&sm.s_free[b]), (c >> 1) & 1);
                     }
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                if (__syncthreads_or(*abort_flag != 0)) { ok = false; break; }
-                if (tid == 0) {
+                if (!ok) break;
+                c1 += x.ns;
+                // only units with query tiles signal their accumulators: each such
+                // commit follows an arrival of the compute warps on the same unit,
+                // so it can never run two phases ahead of their wait
+                if (x.ns > 0) mma_commit(smem_u32(&sm.dv_full));
+                // ---- pass 2
+                for (int s = 0; s < x.ns && ok; ++s) {
+                    const int c = c2 + s;
+                    if (!(ok = settle(pend_s[0]))) break;
+                    if (!(ok = issue_s(0, kaddr))) break;
+                    if (!(ok = settle(pend_s[1]))) break;
+                    if (!(ok = issue_s(128, vaddr))) break;  // dP^T = V dO^T (the dO chunks)
+                    mma_commit(smem_u32(&sm.sdp_full));
+                    if (!(ok = wait_or_abort(smem_u32(&sm.ds_ready), c & 1, abort_flag, hdr))) break;
                     tc_fence_after();
                     // dK += dS^T Q_i, 64 columns of Q per chunk (A = dS^T, K-major)
-                    for (int cc = 0; cc < C; ++cc) {
-                        const uint32_t a = acquire(s * per + 2 * C + cc);
-                        if (!a) break;  // (abort flag raised: every thread stops below)
+                    for (int cc = 0; cc < C && ok; ++cc) {
+                        const uint32_t a = acquire();
+                        if (!(ok = a != 0)) break;
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
                             mma_ss(tmem + kColDKV + cc * 64,
                                    make_sdesc(dsaddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                                    make_sdesc(a + kk * 2048, 16384, 1024), idN,
                                    (s > 0 || kk > 0) ? 1u : 0u);
-                        release(s * per + 2 * C + cc);
+                        release();
                     }
+                    if (!ok) break;
                     // dQ = dS K_j into [0, D): S^T and dP^T have been read
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk)
                         mma_ss(tmem, make_sdesc(dsaddr + kk * 2048, 16384, 1024),
                                make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ, kk > 0);
-                    mma_commit(mbar_mma);
+                    mma_commit(smem_u32(&sm.dq_full));
+                    if (!(ok = expect(pend_s[0], smem_u32(&sm.dq_free[0]), c & 1))) break;
+                    ok = expect(pend_s[1], smem_u32(&sm.dq_free[1]), c & 1);
                 }
-                wait_mma();
-                // dQ merge: this thread's query row of tile i
-                int* sem = nullptr;
-                if (p.deterministic) {
-                    sem = sems + (size_t)h * n_qtiles + tile_off[x.b] + i;
-                    if (tid == 0 && !sem_wait(sem, dq_rank<KV>(x, i, p.causal), hdr))
-                        raise_abort(abort_flag, hdr, kErrTimeout);
+                if (!ok) break;
+                c2 += x.ns;
+                if (x.ns > 0) mma_commit(smem_u32(&sm.dk_full));
+                mma_commit(smem_u32(&sm.kv_empty));  // K and V read by every MMA issued
+            }
+            // never leave an MMA in flight
+            mma_commit(smem_u32(&sm.drain));
+            mbar_wait(smem_u32(&sm.drain), 0, &sm.zero);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ compute
+        const int ct = threadIdx.x - 128;  // key row (P, dS, epilogue) / query row (merge)
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const bool leader = ct == 0;
+        int sched_it = 0, acc_it = 0, c1 = 0, c2 = 0, rs = 0;  // rs: staged row sets
+        // acc_it: units with query tiles (the ones whose dV / dK the MMAs signal)
+        bool ok = true;
+        while (ok) {
+            const int slot = sched_it & 1;
+            if (!(ok = wg_wait(smem_u32(&sm.sched_full[slot]), (sched_it >> 1) & 1, abort_flag, hdr)))
+                break;
+            const int2 unit = sm.sched[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.sched_empty[slot]));
+            ++sched_it;
+            if (unit.x < 0) break;
+            const BUnit x = decode_bunit<KV, false>(unit, p);
+            const int h = x.h0;
+            const int c = x.j * kTile + ct;  // this thread's key row within its sequence
+            const int c_off = c - x.off;
+            const int L_vis = c < x.Lk ? x.L : 0;
+            auto visible = [&](int i, int& lo, int& hi) {
+                if constexpr (KV) {
+                    lo = p.causal ? max(0, c_off - i * kTile) : 0;
+                    hi = min(kTile, L_vis - i * kTile);
+                } else {
+                    lo = p.causal ? max(0, c - i * kTile) : 0;
+                    hi = c < x.L ? min(kTile, x.L - i * kTile) : 0;
                 }
-                if (__syncthreads_or(*abort_flag != 0)) { ok = false; break; }
-                const int row0 = i * kTile;
-                const int qr = row0 + tid;
-                if (row0 + kTile <= x.L) {
-                    // whole tile: bulk tensor reduce-adds of 32 columns, staged
-                    // 128B-swizzled through the dS buffer (dK and dQ have read it)
-                    const uint32_t stage_base = dsaddr;
-                    uint8_t* stage_row = sm.ds + tid * 128;
-                    const int sw = tid & 7;
+            };
+            // LSE (base 2) and D of this thread's query row of tile i
+            auto fetch_rows = [&](int i, float& l2, float& dv) {
+                const int q = i * kTile + ct;
+                l2 = 0.f;
+                dv = 0.f;
+                if (q < x.L) {
+                    const size_t at = (size_t)h * p.T + (size_t)(x.t0 + q);
+                    l2 = p.lse[at] * kLog2e;
+                    dv = p.D[at];
+                }
+            };
+            // dV (pass 1) or dK times scale (pass 2) of this key row, from TMEM
+            auto epilogue = [&](int pass) {
+                const bool valid = c < x.Lk;
+                const size_t tok = (size_t)x.tk0 + (size_t)c;
+                const bool none = x.ns == 0;  // (KV) no query sees the tile: zeros, TMEM not read
+                const float mul = pass == 0 ? 1.f : p.scale;
+                const bool partial = p.nchunks > 1;
 #pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        const int sl = cc & 1;
-                        uint32_t v[32];
-                        tmem_ld32(tmem + lane_off + cc * 32, v);
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t v[32];
+                    if (none) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    } else {
+                        tmem_ld32(tmem + lane_off + kColDKV + cc * 32, v);
                         tmem_ld_wait();
-                        if (tid == 0 && cc >= 2) bulk_wait_group_read<1>();  // the slot's last reduce read it
-                        __syncthreads();
-                        uint8_t* row = stage_row + sl * (kTile * 128);
+                    }
+                    if (!valid) continue;
+                    if (partial) {
+                        float* acc = (pass == 0 ? dv_acc : dk_acc) +
+                                     (tok * (size_t)(p.Hkv * p.nchunks) + x.uh) * D + cc * 32;
+                        float4* d4 = reinterpret_cast<float4*>(acc);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) =
-                                make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                        fence_proxy_async_smem();
-                        __syncthreads();
-                        if (tid == 0) {
-                            tma_reduce_add_3d(&p.tm_dq_acc, stage_base + sl * (kTile * 128), cc * 32,
-                                              h, x.t0 + row0);
-                            bulk_commit_group();
-                        }
+                            d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul,
+                                                __uint_as_float(v[4 * e + 1]) * mul,
+                                                __uint_as_float(v[4 * e + 2]) * mul,
+                                                __uint_as_float(v[4 * e + 3]) * mul);
+                    } else if (p.grad_fp32) {
+                        float* out = static_cast<float*>(pass == 0 ? p.dv : p.dk) +
+                                     (tok * p.Hkv + x.g) * D + cc * 32;
+                        float4* d4 = reinterpret_cast<float4*>(out);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul,
+                                                __uint_as_float(v[4 * e + 1]) * mul,
+                                                __uint_as_float(v[4 * e + 2]) * mul,
+                                                __uint_as_float(v[4 * e + 3]) * mul);
+                    } else {
+                        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(pass == 0 ? p.dv : p.dk) +
+                                             (tok * p.Hkv + x.g) * D + cc * 32;
+                        uint4* d4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            d4[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]) * mul,
+                                                           __uint_as_float(v[8 * e + 1]) * mul),
+                                               pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul,
+                                                           __uint_as_float(v[8 * e + 3]) * mul),
+                                               pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul,
+                                                           __uint_as_float(v[8 * e + 5]) * mul),
+                                               pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul,
+                                                           __uint_as_float(v[8 * e + 7]) * mul));
                     }
-                    // the next step writes dS^T over the staging: its reduces must have read it
-                    if (tid == 0) {
-                        if (p.deterministic) {
-                            bulk_wait_group<0>();
-                            fence_proxy_async_global();
-                        } else {
-                            bulk_wait_group_read<0>();
-                        }
-                    }
-                } else {
-                    // ragged last tile of a sequence: per-row vector reductions
-                    float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + h) * D;
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem + lane_off + cc * 32, v);
+                }
+                tc_fence_before();  // (the next arrival orders these reads before dK / dV)
+            };
+
+            for (int pass = 0; pass < 2 && ok; ++pass) {
+                float nl2 = 0.f, ndd = 0.f;
+                if (x.ns > 0) fetch_rows(walk_tile<KV>(x, 0, p.deterministic, p.causal), nl2, ndd);
+                for (int s = 0; s < x.ns; ++s) {
+                    const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
+                    const int rb = rs++ & 1;  // row buffer: its readers of two steps ago are past
+                    sm.lse2[rb][ct] = nl2;    // the named barrier of the previous step
+                    sm.dd[rb][ct] = ndd;
+                    // (the wait's block-wide vote also publishes the rows)
+                    const uint32_t full_bar =
+                        pass == 0 ? smem_u32(&sm.s_full[(c1 + s) & 1]) : smem_u32(&sm.sdp_full);
+                    const uint32_t full_par = pass == 0 ? ((c1 + s) >> 1) & 1 : (c2 + s) & 1;
+                    if (!(ok = wg_wait(full_bar, full_par, abort_flag, hdr))) break;
+                    tc_fence_after();
+                    if (s + 1 < x.ns)
+                        fetch_rows(walk_tile<KV>(x, s + 1, p.deterministic, p.causal), nl2, ndd);
+                    int lo, hi;
+                    visible(i, lo, hi);
+                    const bool full = lo == 0 && hi == kTile;
+                    if (pass == 0) {
+                        // P^T of this key row, bf16, packed over the first 32 columns of
+                        // each 64-column half of the S^T buffer (query columns
+                        // [64h + 16m, +16) in TMEM columns [64h + 8m, +8)): the A operand of dV
+                        const int b = (c1 + s) & 1;
+                        const uint32_t sb = tmem + lane_off + (uint32_t)b * 128;
+                        uint32_t sv[4][32];
+#pragma unroll
+                        for (int qc = 0; qc < 4; ++qc) tmem_ld32(sb + qc * 32, sv[qc]);
                         tmem_ld_wait();
-                        if (qr < x.L) {
+#pragma unroll
+                        for (int qc = 0; qc < 4; ++qc) {
+                            uint32_t pk[16];
+                            if (full)
+                                p_chunk<false>(sv[qc], sm.lse2[rb] + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                            else
+                                p_chunk<true>(sv[qc], sm.lse2[rb] + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                            tmem_st16(sb + (qc >> 1) * 64 + (qc & 1) * 16, pk);
+                        }
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&sm.p_ready[b]));
+                        continue;
+                    }
+                    // pass 2: dS^T = P^T (dP^T - D), bf16, swizzled rows of the dS^T tile
+                    // (the previous step's dK, dQ and merge staging are done with it)
+                    uint8_t* ds_row = sm.ds + ct * 128;
+                    const int sw = ct & 7;
+#pragma unroll 1
+                    for (int qc = 0; qc < 4; ++qc) {
+                        uint32_t sv[32], dv[32];
+                        tmem_ld32(tmem + lane_off + qc * 32, sv);
+                        tmem_ld32(tmem + lane_off + 128 + qc * 32, dv);
+                        tmem_ld_wait();
+                        uint32_t pk[16];
+                        if (full)
+                            p_chunk<false>(sv, sm.lse2[rb] + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                        else
+                            p_chunk<true>(sv, sm.lse2[rb] + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                        uint32_t out[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 pf =
+                                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[e]));
+                            const float d0 = sm.dd[rb][qc * 32 + 2 * e], d1 = sm.dd[rb][qc * 32 + 2 * e + 1];
+                            out[e] = pack_bf16x2(pf.x * (__uint_as_float(dv[2 * e]) - d0),
+                                                 pf.y * (__uint_as_float(dv[2 * e + 1]) - d1));
+                        }
+                        // 32 query columns = 4 chunks of 16 bytes of half (qc >> 1)'s block
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int ch = (qc & 1) * 4 + e;
+                            *reinterpret_cast<uint4*>(ds_row + (qc >> 1) * 16384 + ((ch ^ sw) << 4)) =
+                                make_uint4(out[4 * e], out[4 * e + 1], out[4 * e + 2], out[4 * e + 3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sm.ds_ready));
+                    // dQ of the step (dK of it issued before)
+                    if (!(ok = wg_wait(smem_u32(&sm.dq_full), (c2 + s) & 1, abort_flag, hdr))) break;
+                    tc_fence_after();
+                    int* sem = nullptr;
+                    bool sem_ok = true;
+                    if (p.deterministic) {
+                        sem = sems + (size_t)h * n_qtiles + tile_off[x.b] + i;
+                        if (leader && !sem_wait(sem, dq_rank<KV>(x, i, p.causal), hdr)) {
+                            raise_abort(abort_flag, hdr, kErrTimeout);
+                            sem_ok = false;
+                        }
+                    }
+                    if (!(ok = named_bar_and(1, 128, sem_ok && *abort_flag == 0))) break;
+                    // dQ merge: this thread's query row of tile i.  The columns [0, 128)
+                    // are released once read (the next S^T), the rest at the end (dP^T).
+                    const int row0 = i * kTile;
+                    const int qr = row0 + ct;
+                    auto release_half = [&](int cc) {
+                        if (cc == 3 || cc == D / 32 - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free[cc == 3 ? 0 : 1]));
+                        }
+                    };
+                    if (row0 + kTile <= x.L) {
+                        // whole tile: bulk tensor reduce-adds of 32 columns, staged
+                        // 128B-swizzled through the dS buffer (dK and dQ have read it)
+                        uint8_t* stage_row = sm.ds + ct * 128;
+#pragma unroll 1
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            const int sl = cc & 1;
+                            uint32_t v[32];
+                            tmem_ld32(tmem + lane_off + cc * 32, v);
+                            tmem_ld_wait();
+                            release_half(cc);
+                            if (leader && cc >= 2) bulk_wait_group_read<1>();  // the slot's last reduce read it
+                            named_bar_sync(1, 128);
+                            uint8_t* row = stage_row + sl * (kTile * 128);
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[4 * e]),
-                                           __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
-                                           __uint_as_float(v[4 * e + 3]));
+                                *reinterpret_cast<uint4*>(row + ((e ^ sw) << 4)) =
+                                    make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                            fence_proxy_async_smem();
+                            named_bar_sync(1, 128);
+                            if (leader) {
+                                tma_reduce_add_3d(&p.tm_dq_acc, dsaddr + sl * (kTile * 128), cc * 32, h,
+                                                  x.t0 + row0);
+                                bulk_commit_group();
+                            }
+                        }
+                        // the next step writes dS^T over the staging: its reduces must
+                        // have read it (the next step's wait publishes this)
+                        if (leader) {
+                            if (p.deterministic) {
+                                bulk_wait_group<0>();
+                                fence_proxy_async_global();
+                            } else {
+                                bulk_wait_group_read<0>();
+                            }
+                        }
+                    } else {
+                        // ragged last tile of a sequence: per-row vector reductions
+                        float* dst = dq_acc + ((size_t)(x.t0 + qr) * p.Hq + h) * D;
+#pragma unroll 1
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t v[32];
+                            tmem_ld32(tmem + lane_off + cc * 32, v);
+                            tmem_ld_wait();
+                            release_half(cc);
+                            if (qr < x.L) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(v[4 * e]),
+                                               __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
+                                               __uint_as_float(v[4 * e + 3]));
+                            }
                         }
                     }
+                    if (p.deterministic) {
+                        __threadfence();  // this contribution before the next one
+                        named_bar_sync(1, 128);
+                        if (leader) red_release_gpu_add(sem, 1);
+                    }
                 }
-                tc_fence_before();
-                if (p.deterministic) __threadfence();  // this contribution before the next one
-                __syncthreads();
-                if (p.deterministic && tid == 0) red_release_gpu_add(sem, 1);
+                if (!ok) break;
+                if (pass == 0) c1 += x.ns; else c2 += x.ns;
+                // the pass's accumulator: dV after pass 1, dK after pass 2
+                if (x.ns > 0) {
+                    if (!(ok = wg_wait(smem_u32(pass == 0 ? &sm.dv_full : &sm.dk_full), acc_it & 1,
+                                       abort_flag, hdr)))
+                        break;
+                    tc_fence_after();
+                }
+                epilogue(pass);
             }
-            if (!ok) break;
-            // epilogue of the pass: dV (pass 1) or dK times scale (pass 2) of this key row
-            const bool valid = c < x.Lk;
-            const size_t tok = (size_t)x.tk0 + (size_t)c;
-            const bool none = x.ns == 0;  // (KV) no query sees the tile: zeros, TMEM not written
-            const float mul = pass == 0 ? 1.f : p.scale;
-            const bool partial = p.nchunks > 1;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + kColDKV + cc * 32, v);
-                tmem_ld_wait();
-                if (!valid) continue;
-                if (none) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
-                }
-                if (partial) {
-                    float* acc = (pass == 0 ? dv_acc : dk_acc) +
-                                 (tok * (size_t)(p.Hkv * p.nchunks) + x.uh) * D + cc * 32;
-                    float4* d4 = reinterpret_cast<float4*>(acc);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul,
-                                            __uint_as_float(v[4 * e + 1]) * mul,
-                                            __uint_as_float(v[4 * e + 2]) * mul,
-                                            __uint_as_float(v[4 * e + 3]) * mul);
-                } else if (p.grad_fp32) {
-                    float* out = static_cast<float*>(pass == 0 ? p.dv : p.dk) +
-                                 (tok * p.Hkv + x.g) * D + cc * 32;
-                    float4* d4 = reinterpret_cast<float4*>(out);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul,
-                                            __uint_as_float(v[4 * e + 1]) * mul,
-                                            __uint_as_float(v[4 * e + 2]) * mul,
-                                            __uint_as_float(v[4 * e + 3]) * mul);
-                } else {
-                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(pass == 0 ? p.dv : p.dk) +
-                                         (tok * p.Hkv + x.g) * D + cc * 32;
-                    uint4* d4 = reinterpret_cast<uint4*>(out);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        d4[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]) * mul,
-                                                       __uint_as_float(v[8 * e + 1]) * mul),
-                                           pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul,
-                                                       __uint_as_float(v[8 * e + 3]) * mul),
-                                           pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul,
-                                                       __uint_as_float(v[8 * e + 5]) * mul),
-                                           pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul,
-                                                       __uint_as_float(v[8 * e + 7]) * mul));
-                }
-            }
-            tc_fence_before();
-            __syncthreads();  // the dK/dV columns are free for the next pass or unit
-            g0 += total;
-            issued = 0;
+            if (x.ns > 0) ++acc_it;
         }
-        if (__syncthreads_or(!ok || *abort_flag != 0)) break;
+        // the staging slots must not be read after the CTA exits
+        if (leader) bulk_wait_group<0>();
     }
 
-    // never leave a TMA write or an MMA in flight, then release TMEM
-    if (tid == 0) {
-        const volatile int* z = &sm.zero;
-        const int last = g0 + issued;  // chunks whose loads were issued
-        for (int e = 0; e < kSlots && e < last; ++e) {
-            const int g = last - 1 - e;
-            mbar_wait(smem_u32(&sm.slot_full[g % kSlots]), (g / kSlots) & 1, z);
-        }
-        if (kv_issued > 0) mbar_wait(smem_u32(&sm.kv_full), (kv_issued - 1) & 1, z);
-        bulk_wait_group<0>();  // no reduce may still read the staging
-        mma_commit(smem_u32(&sm.drain));
-        mbar_wait(smem_u32(&sm.drain), 0, z);
-    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
