@@ -571,7 +571,11 @@ def main():
                     help="time the forward alone (no end-to-end leg, no CPU baseline)")
     ap.add_argument("--deterministic", action="store_true",
                     help="run the backward in deterministic mode whatever the workload's default")
+    ap.add_argument("--atomic", action="store_true",
+                    help="run the backward in atomic mode whatever the workload's default")
     args = ap.parse_args()
+    if args.deterministic and args.atomic:
+        ap.error("--deterministic and --atomic exclude each other")
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -579,6 +583,8 @@ def main():
     w = synth.workloads()[args.workload]
     if args.deterministic:
         w.deterministic = True
+    if args.atomic:
+        w.deterministic = False
     inp = synth.make_workload(w)
 
     if args.impl == "reference":
