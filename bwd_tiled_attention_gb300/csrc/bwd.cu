@@ -1030,6 +1030,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     constexpr uint32_t kColDKV = 256;               // dV (pass 1), then dK (pass 2)
     constexpr uint32_t idS = make_idesc_bf16(128, 128, false, false);
     constexpr uint32_t idN = make_idesc_bf16(128, 64, false, true);
+    constexpr uint32_t idN2 = make_idesc_bf16(128, 128, false, true);  // two adjacent chunks
     constexpr uint32_t idDQ = make_idesc_bf16(128, D, true, true);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.workspace);
@@ -1179,14 +1180,37 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 return r;
             };
             // next chunk of the ring: its shared-memory address once landed, or 0
-            auto acquire = [&]() -> uint32_t {
-                const int slot = g % kSlots;
-                if (!wait_or_abort(smem_u32(&sm.slot_full[slot]), (g / kSlots) & 1, abort_flag, hdr))
+            auto acquire = [&](int ahead = 0) -> uint32_t {
+                const int ga = g + ahead, slot = ga % kSlots;
+                if (!wait_or_abort(smem_u32(&sm.slot_full[slot]), (ga / kSlots) & 1, abort_flag, hdr))
                     return 0u;
                 tc_fence_after();
                 return smem_u32(sm.ring[slot]);
             };
             auto release = [&]() { mma_commit(smem_u32(&sm.slot_free[g++ % kSlots])); };
+            // dV / dK take the chunks' d columns as N: two chunks at once (N = 128)
+            // when they sit in adjacent slots (a group of C chunks starts at a
+            // multiple of C in the ring, so only a group's last chunk at d = 192
+            // goes alone), since N = 64 runs the tensor core at two thirds of its
+            // rate.  issue(col, b_addr, n128) issues one chunk or pair into dK/dV
+            // columns col; returns the chunks taken (0 on abort).
+            auto acc_chunks = [&](int cc, auto&& issue) -> int {
+                const uint32_t a = acquire();
+                if (!a) return 0;
+                if (cc + 1 < C && g % kSlots != kSlots - 1) {
+                    const uint32_t a2 = acquire(1);
+                    if (!a2) return 0;
+                    if (a2 == a + kWideChunkBytes) {
+                        issue(kColDKV + cc * 64, a, true);
+                        release();
+                        release();
+                        return 2;
+                    }
+                }
+                issue(kColDKV + cc * 64, a, false);
+                release();
+                return 1;
+            };
             // S^T = K Q^T over C chunks into TMEM column col (accumulating across chunks)
             auto issue_s = [&](uint32_t col, uint32_t abase) -> bool {
                 for (int cc = 0; cc < C; ++cc) {
@@ -1226,16 +1250,16 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         if (!(ok = wait_or_abort(smem_u32(&sm.p_ready[b]), (c >> 1) & 1, abort_flag, hdr)))
                             break;
                         tc_fence_after();
-                        for (int cc = 0; cc < C && ok; ++cc) {
-                            const uint32_t a = acquire();
-                            if (!(ok = a != 0)) break;
+                        for (int cc = 0; cc < C && ok;) {
+                            const int n = acc_chunks(cc, [&](uint32_t col, uint32_t a, bool n128) {
 #pragma unroll
-                            for (int kk = 0; kk < kTile / 16; ++kk)
-                                mma_ts(tmem + kColDKV + cc * 64,
-                                       tmem + b * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
-                                       make_sdesc(a + kk * 2048, 16384, 1024), idN,
-                                       (s > 1 || kk > 0) ? 1u : 0u);
-                            release();
+                                for (int kk = 0; kk < kTile / 16; ++kk)
+                                    mma_ts(tmem + col, tmem + b * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
+                                           make_sdesc(a + kk * 2048, 16384, 1024), n128 ? idN2 : idN,
+                                           (s > 1 || kk > 0) ? 1u : 0u);
+                            });
+                            ok = n > 0;
+                            cc += n;
                         }
                         if (!ok) break;
                         mma_commit(smem_u32(&sm.s_free[b]));
@@ -1259,16 +1283,17 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     if (!(ok = wait_or_abort(smem_u32(&sm.ds_ready), c & 1, abort_flag, hdr))) break;
                     tc_fence_after();
                     // dK += dS^T Q_i, 64 columns of Q per chunk (A = dS^T, K-major)
-                    for (int cc = 0; cc < C && ok; ++cc) {
-                        const uint32_t a = acquire();
-                        if (!(ok = a != 0)) break;
+                    for (int cc = 0; cc < C && ok;) {
+                        const int n = acc_chunks(cc, [&](uint32_t col, uint32_t a, bool n128) {
 #pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss(tmem + kColDKV + cc * 64,
-                                   make_sdesc(dsaddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                                   make_sdesc(a + kk * 2048, 16384, 1024), idN,
-                                   (s > 0 || kk > 0) ? 1u : 0u);
-                        release();
+                            for (int kk = 0; kk < kTile / 16; ++kk)
+                                mma_ss(tmem + col,
+                                       make_sdesc(dsaddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                                       make_sdesc(a + kk * 2048, 16384, 1024), n128 ? idN2 : idN,
+                                       (s > 0 || kk > 0) ? 1u : 0u);
+                        });
+                        ok = n > 0;
+                        cc += n;
                     }
                     if (!ok) break;
                     // dQ = dS K_j into [0, D): S^T and dP^T have been read
