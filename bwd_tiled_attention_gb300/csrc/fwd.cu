@@ -90,8 +90,9 @@ struct FwdSmem {
     alignas(8) uint64_t sched_full[2], sched_empty[2];
     uint64_t q_full, q_empty;
     uint64_t k_full[FwdCfg<D>::kStages], v_full[FwdCfg<D>::kVSlots], kv_empty[FwdCfg<D>::kStages];
-    // D > 128: K and the V slots are released separately
-    uint64_t k_empty1, v_empty[D > 128 ? FwdCfg<D>::kVSlots : 1];
+    // D > 128: K is released box by box (a 64-column box once the S MMAs that
+    // read it are done), the V slots one by one
+    uint64_t k_empty[D > 128 ? FwdCfg<D>::kBoxes : 1], v_empty[D > 128 ? FwdCfg<D>::kVSlots : 1];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
     uint64_t drain;
     int2 sched[2];
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         for (int s = 0; s < Cfg::kVSlots; ++s) mbar_init(smem_u32(&sm.v_full[s]), 1);
         if constexpr (D > 128) {
-            mbar_init(smem_u32(&sm.k_empty1), 1);
+            for (int c = 0; c < Cfg::kBoxes; ++c) mbar_init(smem_u32(&sm.k_empty[c]), 1);
             for (int s = 0; s < Cfg::kVSlots; ++s) mbar_init(smem_u32(&sm.v_empty[s]), 1);
         }
         mbar_init(smem_u32(&sm.drain), 1);
@@ -353,18 +354,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if constexpr (D > 128) {
                     // K runs one tile ahead of V, in the order the MMA thread
                     // consumes them (S(j+1) is issued before PV(j)): iteration j
-                    // loads K(j) once S(j-1) has read the K stage, then the chunks
-                    // of V(j-1), each once its slot's previous chunk has been read.
+                    // loads K(j), each 64-column box as soon as S(j-1)'s MMAs over
+                    // it are done (so only the last box's load follows the whole
+                    // of S(j-1)), then the chunks of V(j-1), each once its slot's
+                    // previous chunk has been read.
                     for (int j = 0; j <= x.nkv && ok; ++j) {
                         if (j < x.nkv) {
-                            if (!(ok = wait_or_abort(smem_u32(&sm.k_empty1), (k_it & 1) ^ 1,
-                                                     abort_flag, hdr)))
-                                break;
                             const uint32_t kb = smem_u32(&sm.k_full[0]);
-                            mbar_arrive_expect_tx(kb, Cfg::kTileBytes);
-                            for (int c = 0; c < Cfg::kBoxes; ++c)
+                            for (int c = 0; c < Cfg::kBoxes && ok; ++c) {
+                                if (!(ok = wait_or_abort(smem_u32(&sm.k_empty[c]), (k_it & 1) ^ 1,
+                                                         abort_flag, hdr)))
+                                    break;
+                                // armed once S(j-1) has begun, so K(j-1) has landed and
+                                // its phase of k_full is complete
+                                if (c == 0) mbar_arrive_expect_tx(kb, Cfg::kTileBytes);
                                 tma_load_3d(smem_u32(sm.k[0]) + c * 16384, &p.tm_k, kb, c * 64,
                                             x.g, x.tk0 + j * kTile);
+                            }
+                            if (!ok) break;
                             ++k_it;
                         }
                         for (int h = 0; j >= 1 && h < Cfg::kVChunks && ok; ++h) {
@@ -468,11 +475,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                                     mma_ss(tmem + b * 128, make_sdesc(qa + off, 16, 1024),
                                            make_sdesc(kb + off, 16, 1024), idS, kk > 0);
+                                    // K's box kk / 4 is read once its four MMAs are done
+                                    if ((kk & 3) == 3) mma_commit(smem_u32(&sm.k_empty[kk >> 2]));
                                 }
                                 mma_commit(smem_u32(&sm.s_full[b]));
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < Cfg::kBoxes; ++c)
+                                    mma_commit(smem_u32(&sm.k_empty[c]));
                             }
                             if (j == x.nkv - 1) mma_commit(smem_u32(&sm.q_empty));
-                            mma_commit(smem_u32(&sm.k_empty1));
                             ++k_it;
                         }
                         if (j >= 1) {

@@ -22,9 +22,10 @@ Layouts modelled:
 
 - d <= 128: two query tiles per unit, a K/V ring of 2 or 4 stages, P written
   over S_t, one O per tile.
-- d = 256: one query tile, S double-buffered, K one tile ahead of V, V in two
-  128-column chunks over 3 slots, P over its S buffer, O stored by the
-  epilogue warps.
+- d = 256: one query tile, S double-buffered, K one tile ahead of V and
+  released box by box (each 64-column box reloaded once the S MMAs over it
+  are done), V in two 128-column chunks over 3 slots, P over its S buffer, O
+  stored by the epilogue warps.
 - d = 192: as d = 256 but with whole V tiles over 2 slots and P in TMEM
   columns of its own.
 
@@ -379,17 +380,17 @@ def test_two_tile_planted_mistakes(mistake, warps):
 
 # ------------------------------------------------------------------ d > 128
 
-def run_one_tile(units, seed, nv, slots, sep_p, mistake=None, warps=1):
+def run_one_tile(units, seed, nv, slots, sep_p, nb, mistake=None, warps=1):
     """units: list of (n, nkv): steps with MMAs (0: no row sees a key), and
-    key/value tiles loaded (>= 1).  warps: the softmax and the epilogue
-    warpgroups as one actor each (1), or as four warps arriving on their own
-    (4), each owning a quarter of the rows."""
+    key/value tiles loaded (>= 1).  nb: 64-column boxes of a K tile.  warps:
+    the softmax and the epilogue warpgroups as one actor each (1), or as four
+    warps arriving on their own (4), each owning a quarter of the rows."""
     sim = Sim(units, seed, consumers=1 + 2 * warps)  # MMA issuer + softmax + epilogue warps
     for i in (0, 1):
         sim.bar(f"s_full{i}")
         sim.bar(f"o_done{i}")
         sim.bar(f"p_full{i}", warps)
-    for name in ("q_full", "q_empty", "k_full", "k_empty"):
+    for name in ["q_full", "q_empty", "k_full"] + [f"k_empty{c}" for c in range(nb)]:
         sim.bar(name)
     for name in ("o_free", "ep_full"):
         sim.bar(name, warps)
@@ -417,9 +418,17 @@ def run_one_tile(units, seed, nv, slots, sep_p, mistake=None, warps=1):
             it_unit += 1
             for j in range(nkv + 1):
                 if j < nkv:
-                    while not sim.ready("k_empty", (k_it & 1) ^ 1, k_it):
+                    if mistake == "k_arm_early":
+                        sim.bars["k_full"].expect_tx(nb)
+                    for c in range(nb):
+                        if c == 0 or mistake != "no_k_box_wait":
+                            while not sim.ready(f"k_empty{c}", (k_it & 1) ^ 1, k_it):
+                                yield
+                        if c == 0 and mistake != "k_arm_early":
+                            # armed once the previous tile's phase is complete
+                            sim.bars["k_full"].expect_tx(nb)
+                        sim.issue("k_full", f"k{c}", (uid, j))
                         yield
-                    sim.load("k_full", "k", (uid, j))
                     k_it += 1
                 for h in range(nv if j >= 1 else 0):
                     s = v_it % slots
@@ -453,11 +462,18 @@ def run_one_tile(units, seed, nv, slots, sep_p, mistake=None, warps=1):
                         if not sep_p and gj >= 2 and mistake != "no_s_buffer_wait":
                             while not sim.ready(f"o_done{b}", ((gj - 2) >> 1) & 1, ((gj - 2) >> 1) + 1):
                                 yield
-                        sim.pipe.append(("S", (uid, j, b)))
+                        for c in range(nb):
+                            if mistake == "k_box_release_early":
+                                sim.pipe.append(("commit", f"k_empty{c}"))
+                            sim.pipe.append(("S", (uid, j, b, c)))
+                            if mistake != "k_box_release_early":
+                                sim.pipe.append(("commit", f"k_empty{c}"))
                         sim.pipe.append(("commit", f"s_full{b}"))
+                    else:
+                        for c in range(nb):
+                            sim.pipe.append(("commit", f"k_empty{c}"))
                     if j == nkv - 1:
                         sim.pipe.append(("commit", "q_empty"))
-                    sim.pipe.append(("commit", "k_empty"))
                     k_it += 1
                 if j >= 1:
                     jp = j - 1
@@ -558,16 +574,19 @@ def run_one_tile(units, seed, nv, slots, sep_p, mistake=None, warps=1):
         elif op == "skip_v":
             st["v_read"][arg] = True
         elif op == "S":
-            uid, j, b = arg
-            if smem.get("q") != uid or smem.get("k") != (uid, j):
-                raise Hazard(f"S ({uid},{j}) read Q {smem.get('q')}, K {smem.get('k')}")
-            if b in st["S"] and len(st["S_read"].get(b, ())) < warps:
-                raise Hazard(f"S ({uid},{j}) overwrote unread scores {st['S'][b]}")
-            if not sep_p and any(v != "read" for v in st["P"].get(b, {}).values()):
-                raise Hazard(f"S ({uid},{j}) overwrote P {st['P'][b]} before PV read it")
-            st["S"][b], st["S_read"][b] = (uid, j), set()
-            if not sep_p:
-                st["P"][b] = {}
+            # the MMAs over K's box c (the first one starts overwriting S_b)
+            uid, j, b, c = arg
+            if smem.get("q") != uid or smem.get(f"k{c}") != (uid, j):
+                raise Hazard(f"S ({uid},{j}) box {c} read Q {smem.get('q')}, K {smem.get(f'k{c}')}")
+            if c == 0:
+                if b in st["S"] and len(st["S_read"].get(b, ())) < warps:
+                    raise Hazard(f"S ({uid},{j}) overwrote unread scores {st['S'][b]}")
+                if not sep_p and any(v != "read" for v in st["P"].get(b, {}).values()):
+                    raise Hazard(f"S ({uid},{j}) overwrote P {st['P'][b]} before PV read it")
+                if not sep_p:
+                    st["P"][b] = {}
+            st["S"][b] = (uid, j) if c == nb - 1 else ("partial", uid, j)
+            st["S_read"][b] = set()
         elif op == "PV":
             uid, j, b, h, s = arg
             p_at = "sep" if sep_p else b
@@ -598,7 +617,8 @@ def random_one_tile_units(rnd):
     return units
 
 
-ONE_TILE = {"d256": dict(nv=2, slots=3, sep_p=False), "d192": dict(nv=1, slots=2, sep_p=True)}
+ONE_TILE = {"d256": dict(nv=2, slots=3, sep_p=False, nb=4),
+            "d192": dict(nv=1, slots=2, sep_p=True, nb=3)}
 
 
 @pytest.mark.parametrize("warps", [1, 4])
@@ -612,8 +632,13 @@ def test_one_tile_protocol_is_hazard_and_deadlock_free(cfg, warps):
 # As above; no_s_buffer_wait is implied by an in-order tensor pipe (S(j)
 # runs after PV(j-2) anyway), which the kernel does not rely on.  Here the
 # epilogue warps store O, so the first PV of a unit must wait for them.
+# no_k_box_wait: K's boxes after the first loaded without waiting for their
+# release; k_box_release_early: a box released before its S MMAs; k_arm_early:
+# k_full armed for the next tile before the first box is free, possibly
+# inside the phase of the tile still landing.
 ONE_TILE_MISTAKES = {"no_s_buffer_wait": False, "no_v_slot_wait": True, "no_pv_wait": True,
-                     "no_stats_wait": True, "no_o_free_wait": True}
+                     "no_stats_wait": True, "no_o_free_wait": True, "no_k_box_wait": True,
+                     "k_box_release_early": True, "k_arm_early": True}
 
 
 @pytest.mark.parametrize("warps", [1, 4])
