@@ -247,8 +247,11 @@ __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
 }
 
 // Bounded wait until *sem == target (or some CTA already recorded an error).
+// The first polls follow each other back to back (the wait is on the dQ
+// chain, where each poll's latency counts); later ones sleep between polls.
 __device__ bool sem_wait(const int* sem, int target, const WsHeader* hdr) {
-    if (ld_acquire_gpu(sem) == target) return true;
+    for (int i = 0; i < 64; ++i)
+        if (ld_acquire_gpu(sem) == target) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         for (int i = 0; i < 16; ++i) {
@@ -856,14 +859,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                        __uint_as_float(v[cc][4 * e + 3]));
                 }
                 if (p.deterministic) {
-                    // this contribution must be complete before the next one may start
-                    if (leader) {
-                        bulk_wait_group<0>();
-                        fence_proxy_async_global();
+                    // this contribution must be complete before the next one may start:
+                    // a whole tile's reduce-adds are the leader's own bulk operations;
+                    // a ragged tile's vector reductions are every thread's
+                    if (whole) {
+                        if (leader) {
+                            bulk_wait_group<0>();
+                            fence_proxy_async_global();
+                            if (sem_ok) red_release_gpu_add(sem, 1);
+                        }
+                    } else {
+                        __threadfence();
+                        named_bar_sync(1, 128);
+                        if (leader && sem_ok) red_release_gpu_add(sem, 1);
                     }
-                    __threadfence();
-                    named_bar_sync(1, 128);
-                    if (leader && sem_ok) red_release_gpu_add(sem, 1);
                 }
                 ++cnt;
                 if (!sem_ok) { ok = false; break; }
