@@ -288,9 +288,10 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* l
 }
 
 // D: the tile layout (64 or 128 columns); DR: the head dimension in memory.
-// DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros,
-// which add nothing to S or dP and make the last 32 columns of dV, dK and dQ
-// zero; those columns are neither stored nor merged.
+// DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros.
+// S and dP contract over the first 96 columns only (6 MMAs of K = 16).  dV, dK
+// and dQ keep N = 128 (their B operands are read MN-major in 64-column swizzle
+// atoms); their last 32 columns are zero and neither stored nor merged.
 template <int D, int DR, bool KV, bool RUNS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
@@ -496,7 +497,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 const uint32_t qaddr = smem_u32(sm.q[c & 1]);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < DR / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                     mma_ss(tmem + Cfg::kColS, make_sdesc(kaddr + off, 16, 1024),
                            make_sdesc(qaddr + off, 16, 1024), idS, kk > 0);
@@ -535,7 +536,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  mbar_test_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
                                 tc_fence_after();
 #pragma unroll
-                                for (int kk = 0; kk < D / 16; ++kk) {
+                                for (int kk = 0; kk < DR / 16; ++kk) {
                                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                                     mma_ss(tmem + Cfg::kColDP, make_sdesc(vaddr + off, 16, 1024),
                                            make_sdesc(doaddr + off, 16, 1024), idS, kk > 0);
@@ -602,7 +603,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 tc_fence_after();
                                 const uint32_t qn = smem_u32(sm.q[(cnt + 1) & 1]);
 #pragma unroll
-                                for (int kk = 0; kk < D / 16; ++kk) {
+                                for (int kk = 0; kk < DR / 16; ++kk) {
                                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                                     mma_ss(tmem + Cfg::kColS, make_sdesc(kaddr + off, 16, 1024),
                                            make_sdesc(qn + off, 16, 1024), idS, kk > 0);

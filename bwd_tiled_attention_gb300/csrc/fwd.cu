@@ -251,8 +251,10 @@ __device__ __forceinline__ void store_row(const FwdParams& p, uint32_t o_addr, i
 
 // D: the tile layout (64, 128, 192 or 256 columns); DR: the head dimension in
 // memory.
-// DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros,
-// which add nothing to S, and O's last 32 columns (all zero) are not stored.
+// DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros.
+// S contracts over the first 96 columns only (6 MMAs of K = 16); PV keeps
+// N = 128 (V is read MN-major in 64-column swizzle atoms), and O's last 32
+// columns (all zero) are not stored.
 template <int D, int DR, bool OUT_FP32, bool KV>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
@@ -542,7 +544,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             tc_fence_after();
                             const uint32_t qa = smem_u32(sm.q[t]), kb = smem_u32(sm.k[st]);
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
+                            for (int kk = 0; kk < DR / 16; ++kk) {  // (columns past DR are zero)
                                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                                 mma_ss(tmem + t * 128, make_sdesc(qa + off, 16, 1024),
                                        make_sdesc(kb + off, 16, 1024), idS, kk > 0);
