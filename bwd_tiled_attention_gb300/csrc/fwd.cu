@@ -94,6 +94,9 @@ struct FwdSmem {
     // read it are done), the V slots one by one
     uint64_t k_empty[D > 128 ? FwdCfg<D>::kBoxes : 1], v_empty[D > 128 ? FwdCfg<D>::kVSlots : 1];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+    // d <= 128: P_t in two halves, keys [0, 64) (p_full) and [64, 128) (p_hi),
+    // so PV_t's first four MMAs run while the softmax computes the second half
+    uint64_t p_hi[2];
     uint64_t drain;
     int2 sched[2];
     uint32_t tmem_base;
@@ -276,6 +279,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(smem_u32(&sm.sched_empty[i]), 1 + 8);
             mbar_init(smem_u32(&sm.s_full[i]), 1);
             mbar_init(smem_u32(&sm.p_full[i]), 4);
+            mbar_init(smem_u32(&sm.p_hi[i]), 4);
             mbar_init(smem_u32(&sm.o_done[i]), 1);
             mbar_init(smem_u32(&sm.o_free[i]), 4);
         }
@@ -569,11 +573,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             tc_fence_after();
                             const uint32_t vb = smem_u32(sm.v[st]);
                             const uint32_t o_col = 256 + t * 128, p_col = t * 128;
+                            // keys [0, 64) of P_t, then [64, 128) once the softmax has them
 #pragma unroll
-                            for (int kk = 0; kk < kTile / 16; ++kk)
+                            for (int kk = 0; kk < kTile / 16; ++kk) {
+                                if (kk == kTile / 32) {
+                                    if (!(ok = wait_or_abort(smem_u32(&sm.p_hi[t]), it[t] & 1,
+                                                             abort_flag, hdr)))
+                                        break;
+                                    tc_fence_after();
+                                }
                                 mma_ts(tmem + o_col, tmem + p_col + kk * 8,
                                        make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
                                        (j > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            if (!ok) break;
                             mma_commit(smem_u32(&sm.o_done[t]));
                             ++it[t];
                         }
@@ -710,6 +723,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
                 const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
                 uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+                if constexpr (D <= 128) {
+                    // O~ first (stable: S_t(j) was committed after O_t += P_t V of
+                    // j - 1), then P in two halves, each handed over as soon as it is
+                    // in TMEM: PV_t may start on keys [0, 64) while the exponentials
+                    // of [64, 128) run.  (All of S_t is in registers, so P's first
+                    // columns may overwrite it.)
+                    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                        for (int c = 0; c < DR / 32; ++c) {
+                            uint32_t ov[32];
+                            tmem_ld32(o_addr + c * 32, ov);
+                            tmem_ld_wait();
+                            uint32_t lo[16], hi[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                lo[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                                hi[i] = __float_as_uint(__uint_as_float(ov[16 + i]) * alpha);
+                            }
+                            tmem_st16(o_addr + c * 32, lo);
+                            tmem_st16(o_addr + c * 32 + 16, hi);
+                        }
+                    }
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                        for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
+                            uint32_t pk[16];
+                            softmax_chunk(s + c * 32, p.scale_log2, neg, acc, pk);
+                            tmem_st16(s_at + c * 16, pk);
+                        }
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(hf == 0 ? &sm.p_full[buf] : &sm.p_hi[buf]));
+                    }
+                    float a0, a1, b0, b1;
+                    f2_unpack(acc[0], a0, a1);
+                    f2_unpack(acc[1], b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                    ++it;
+                    continue;
+                }
                 if constexpr (Cfg::kSepP) {
                     // P has a region of its own: compute it in registers, then store
                     // it once PV(it - 1) has read the previous P (which also makes

@@ -21,7 +21,8 @@ expects. A run that stops making progress is a deadlock.
 Layouts modelled:
 
 - d <= 128: two query tiles per unit, a K/V ring of 2 or 4 stages, P written
-  over S_t, one O per tile.
+  over S_t in two halves (keys [0, 64) and [64, 128)), each handed to the MMA
+  issuer on its own so that PV_t runs in two halves, one O per tile.
 - d = 256: one query tile, S double-buffered, K one tile ahead of V and
   released box by box (each 64-column box reloaded once the S MMAs over it
   are done), V in two 128-column chunks over 3 slots, P over its S buffer, O
@@ -168,7 +169,7 @@ def run_two_tile(units, seed, stages, mistake=None, warps=1):
     for t in (0, 1):
         for name in ("s_full", "o_done"):
             sim.bar(f"{name}{t}")
-        for name in ("p_full", "o_free"):
+        for name in ("p_full", "p_hi", "o_free"):
             sim.bar(f"{name}{t}", warps)
     for name in ("q_full", "q_empty"):
         sim.bar(name)
@@ -247,7 +248,11 @@ def run_two_tile(units, seed, stages, mistake=None, warps=1):
                     if j == 0 and ep[t] > 0 and mistake != "no_o_free_wait":
                         while not sim.ready(f"o_free{t}", (ep[t] - 1) & 1, ep[t]):
                             yield
-                    sim.pipe.append(("PV", (uid, t, j, s)))
+                    sim.pipe.append(("PV", (uid, t, j, s, 0)))  # keys [0, 64)
+                    if mistake != "no_p_hi_wait":
+                        while not sim.ready(f"p_hi{t}", it[t] & 1, it[t] + 1):
+                            yield
+                    sim.pipe.append(("PV", (uid, t, j, s, 1)))  # keys [64, 128)
                     sim.pipe.append(("commit", f"o_done{t}"))
                     it[t] += 1
                 sim.pipe.append(("kv_read", s))
@@ -274,19 +279,27 @@ def run_two_tile(units, seed, stages, mistake=None, warps=1):
                     yield
                 if st["S"].get(t) != (uid, j):
                     raise Hazard(f"softmax {t}.{w} ({uid},{j}) read S = {st['S'].get(t)}")
-                yield  # the exponentials
+                yield  # the row maximum (all of S_t is now in registers)
                 if st["S"].get(t) != (uid, j):
                     raise Hazard("S overwritten while the softmax read it")
-                st["P"].setdefault(t, {})[w] = (uid, j)
-                if j > 0 and sim.rnd.random() < 0.3 and st["O"][t] != [(uid, q) for q in range(j)]:
+                done = [(uid, q, h) for q in range(j) for h in (0, 1)]
+                rescale = j > 0 and sim.rnd.random() < 0.3
+                if rescale and mistake != "rescale_after_p" and st["O"][t] != done:
                     raise Hazard(f"rescale of tile {t} ({uid},{j}) saw O = {st['O'][t]}")
-                sim.bars[f"p_full{t}"].arrive((uid, j))
+                for hf, bar in ((0, "p_full"), (1, "p_hi")):
+                    yield  # the exponentials of this half
+                    st["P"].setdefault((t, hf), {})[w] = (uid, j)
+                    sim.bars[f"{bar}{t}"].arrive((uid, j))
+                    if hf == 0 and rescale and mistake == "rescale_after_p":
+                        yield
+                        if st["O"][t] != done:
+                            raise Hazard(f"rescale of tile {t} ({uid},{j}) saw O = {st['O'][t]}")
                 it += 1
                 yield
             while not sim.ready(f"o_done{t}", (it - 1) & 1, it):
                 yield
             for _ in range(2):  # reads O over a while
-                if st["O"][t] != [(uid, q) for q in range(nt)]:
+                if st["O"][t] != [(uid, q, h) for q in range(nt) for h in (0, 1)]:
                     raise Hazard(f"epilogue of tile {t} of {uid} read O = {st['O'][t]}")
                 yield
             if w == 0:
@@ -304,19 +317,21 @@ def run_two_tile(units, seed, stages, mistake=None, warps=1):
             uid, t, j, s = arg
             if smem.get(f"q{t}") != uid or smem.get(f"k{s}") != (uid, j):
                 raise Hazard(f"S_{t} ({uid},{j}) read Q {smem.get(f'q{t}')}, K {smem.get(f'k{s}')}")
-            if any(v != "read" for v in st["P"].get(t, {}).values()):
-                raise Hazard(f"S_{t} ({uid},{j}) overwrote P {st['P'][t]} before PV read it")
-            st["S"][t], st["P"][t] = (uid, j), {}
+            for hf in (0, 1):
+                if any(v != "read" for v in st["P"].get((t, hf), {}).values()):
+                    raise Hazard(f"S_{t} ({uid},{j}) overwrote P {st['P'][(t, hf)]} before PV read it")
+                st["P"][(t, hf)] = {}
+            st["S"][t] = (uid, j)
         elif op == "PV":
-            uid, t, j, s = arg
-            quarters = st["P"].get(t, {})
+            uid, t, j, s, hf = arg
+            quarters = st["P"].get((t, hf), {})
             if smem.get(f"v{s}") != (uid, j) or len(quarters) != warps or any(
                     v != (uid, j) for v in quarters.values()):
-                raise Hazard(f"PV_{t} ({uid},{j}) read V {smem.get(f'v{s}')}, P {quarters}")
-            if j == 0:
+                raise Hazard(f"PV_{t} ({uid},{j}) half {hf} read V {smem.get(f'v{s}')}, P {quarters}")
+            if j == 0 and hf == 0:
                 st["O"][t] = []
-            st["O"][t].append((uid, j))
-            st["P"][t] = {q: "read" for q in quarters}
+            st["O"][t].append((uid, j, hf))
+            st["P"][(t, hf)] = {q: "read" for q in quarters}
 
     roles = [producer(), mma()] + [softmax(t, w) for t in (0, 1) for w in range(warps)]
     sim.run(roles, execute, smem)
@@ -360,8 +375,12 @@ def test_two_tile_protocol_is_hazard_and_deadlock_free(stages, warps):
 #   anyway; the kernel does not rely on that order.
 # - no_o_free_wait: the warpgroup that stores O_t is the one whose next P_t
 #   the first PV_t of the next unit waits for.
+# - no_p_hi_wait: PV_t's second half issued without waiting for the second
+#   half of P;
+# - rescale_after_p: the O~ rescale done after the first half of P is handed
+#   over, when PV_t's first half may already be adding into O.
 TWO_TILE_MISTAKES = {"no_s_wait": False, "no_o_free_wait": False, "no_kv_empty_wait": True,
-                     "no_q_empty_wait": True}
+                     "no_q_empty_wait": True, "no_p_hi_wait": True, "rescale_after_p": True}
 
 
 @pytest.mark.parametrize("warps", [1, 4])
