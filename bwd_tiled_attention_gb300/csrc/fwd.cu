@@ -25,7 +25,9 @@
 // feeds two MMAs, and the tensor core works on one tile while the softmax
 // warps of the other tile run.  TMEM: S_0 [0,128), S_1 [128,256), O_0
 // [256,256+d), O_1 [384,384+d); P_t is written as bf16 over the first 64
-// columns of S_t.  Head dimensions above 128 leave room for one query tile
+// columns of S_t, in two halves (keys [0, 64), then [64, 128)), each handed
+// to the MMA issuer on its own, so PV_t starts on the first half while the
+// softmax computes the second.  Head dimensions above 128 leave room for one query tile
 // (O takes [256,256+d)); its S is then double-buffered over [0,256): S(j+1)
 // is issued before O += P(j) V, so the tensor core computes the next scores
 // while the softmax warps work on the current ones, and warps 8..11 store O.
