@@ -96,8 +96,8 @@ struct FwdSmem {
     // read it are done), the V slots one by one
     uint64_t k_empty[D > 128 ? FwdCfg<D>::kBoxes : 1], v_empty[D > 128 ? FwdCfg<D>::kVSlots : 1];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
-    // d <= 128: P_t in two halves, keys [0, 64) (p_full) and [64, 128) (p_hi),
-    // so PV_t's first four MMAs run while the softmax computes the second half
+    // P in two halves, keys [0, 64) (p_full) and [64, 128) (p_hi), so PV's
+    // first four MMAs run while the softmax computes the second half
     uint64_t p_hi[2];
     uint64_t drain;
     int2 sched[2];
@@ -516,12 +516,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                 if (jp < n) {
                                     tc_fence_after();
                                     const uint32_t vb = smem_u32(sm.v[slot]);
+                                    // the first chunk starts on keys [0, 64) of P and waits
+                                    // for [64, 128) halfway
 #pragma unroll
-                                    for (int kk = 0; kk < kTile / 16; ++kk)
+                                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                                        if (h == 0 && kk == kTile / 32) {
+                                            if (!(ok = wait_or_abort(smem_u32(&sm.p_hi[b]), (gj >> 1) & 1,
+                                                                     abort_flag, hdr)))
+                                                break;
+                                            tc_fence_after();
+                                        }
                                         mma_ts(tmem + 256 + h * Cfg::kVChunk,
                                                tmem + (Cfg::kSepP ? Cfg::kPCol : b * 128) + kk * 8,
                                                make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
                                                (jp > 0 || kk > 0) ? 1u : 0u);
+                                    }
+                                    if (!ok) break;
                                 }
                                 mma_commit(smem_u32(&sm.v_empty[slot]));
                                 ++v_it;
@@ -767,43 +777,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     ++it;
                     continue;
                 }
-                if constexpr (Cfg::kSepP) {
-                    // P has a region of its own: compute it in registers, then store
-                    // it once PV(it - 1) has read the previous P (which also makes
-                    // O~ stable for the rescale below)
-                    uint32_t pk[4][16];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) softmax_chunk(s + c * 32, p.scale_log2, neg, acc, pk[c]);
-                    if (it > 0 && !(ok = warp_wait(smem_u32(&sm.o_done[(it - 1) & 1]),
-                                                   ((it - 1) >> 1) & 1, abort_flag, hdr)))
+                // One tile (D > 128): S(j) may finish before PV(j-1), so O~ is
+                // stable only once PV(j-1) is done (j >= 1 whenever a rescale is
+                // needed).  The rescale comes first, then P in two halves as for
+                // two tiles; with P in columns of its own (d = 192) each half is
+                // computed in registers before it waits for PV(j-1) to have read
+                // the previous P.
+                bool pv_done = it == 0;
+                if (__any_sync(0xffffffffu, need)) {
+                    if (!(ok = warp_wait(smem_u32(&sm.o_done[(it - 1) & 1]), ((it - 1) >> 1) & 1,
+                                         abort_flag, hdr)))
                         break;
                     tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_st16(tmem + lane_off + Cfg::kPCol + c * 16, pk[c]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t pk[16];
-                        softmax_chunk(s + c * 32, p.scale_log2, neg, acc, pk);
-                        tmem_st16(s_at + c * 16, pk);
-                    }
-                }
-                {
-                    float a0, a1, b0, b1;
-                    f2_unpack(acc[0], a0, a1);
-                    f2_unpack(acc[1], b0, b1);
-                    l += (a0 + a1) + (b0 + b1);
-                }
-                if (__any_sync(0xffffffffu, need)) {
-                    // O~ must be stable.  Two query tiles: S_t(j) was committed after
-                    // O_t += P_t V of j-1.  One tile (D > 128): S(j) may finish first,
-                    // so wait for PV(j-1) (j >= 1 whenever a rescale is needed).
-                    if constexpr (D > 128 && !Cfg::kSepP) {
-                        if (!(ok = warp_wait(smem_u32(&sm.o_done[(it - 1) & 1]), ((it - 1) >> 1) & 1,
-                                             abort_flag, hdr)))
-                            break;
-                        tc_fence_after();
-                    }
+                    pv_done = true;
 #pragma unroll 1
                     for (int c = 0; c < DR / 32; ++c) {
                         uint32_t ov[32];
@@ -819,10 +805,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         tmem_st16(o_addr + c * 32 + 16, hi);
                     }
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[buf]));
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    if constexpr (Cfg::kSepP) {
+                        uint32_t pk[2][16];
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            softmax_chunk(s + (2 * hf + c) * 32, p.scale_log2, neg, acc, pk[c]);
+                        if (!pv_done) {
+                            if (!(ok = warp_wait(smem_u32(&sm.o_done[(it - 1) & 1]),
+                                                 ((it - 1) >> 1) & 1, abort_flag, hdr)))
+                                break;
+                            tc_fence_after();
+                            pv_done = true;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tmem_st16(tmem + lane_off + Cfg::kPCol + (2 * hf + c) * 16, pk[c]);
+                    } else {
+#pragma unroll
+                        for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
+                            uint32_t pk[16];
+                            softmax_chunk(s + c * 32, p.scale_log2, neg, acc, pk);
+                            tmem_st16(s_at + c * 16, pk);
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(hf == 0 ? &sm.p_full[buf] : &sm.p_hi[buf]));
+                }
+                if (!ok) break;
+                {
+                    float a0, a1, b0, b1;
+                    f2_unpack(acc[0], a0, a1);
+                    f2_unpack(acc[1], b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                }
                 ++it;
             }
             if (!ok) break;

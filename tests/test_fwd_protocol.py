@@ -408,7 +408,8 @@ def run_one_tile(units, seed, nv, slots, sep_p, nb, mistake=None, warps=1):
     for i in (0, 1):
         sim.bar(f"s_full{i}")
         sim.bar(f"o_done{i}")
-        sim.bar(f"p_full{i}", warps)
+        sim.bar(f"p_full{i}", warps)  # P's first half (keys [0, 64))
+        sim.bar(f"p_hi{i}", warps)    # P's second half
     for name in ["q_full", "q_empty", "k_full"] + [f"k_empty{c}" for c in range(nb)]:
         sim.bar(name)
     for name in ("o_free", "ep_full"):
@@ -508,7 +509,15 @@ def run_one_tile(units, seed, nv, slots, sep_p, nb, mistake=None, warps=1):
                         s = v_it % slots
                         while not sim.ready(f"v_full{s}", (v_it // slots) & 1, v_it // slots + 1):
                             yield
-                        sim.pipe.append(("PV", (uid, jp, b, h, s)) if jp < n else ("skip_v", s))
+                        if jp < n:
+                            # the first chunk waits for P's second half halfway
+                            sim.pipe.append(("PV", (uid, jp, b, h, s, 0)))
+                            if h == 0 and mistake != "no_p_hi_wait":
+                                while not sim.ready(f"p_hi{b}", (gj >> 1) & 1, (gj >> 1) + 1):
+                                    yield
+                            sim.pipe.append(("PV", (uid, jp, b, h, s, 1)))
+                        else:
+                            sim.pipe.append(("skip_v", s))
                         sim.pipe.append(("commit", f"v_empty{s}"))
                         v_it += 1
                     if jp < n:
@@ -536,22 +545,34 @@ def run_one_tile(units, seed, nv, slots, sep_p, nb, mistake=None, warps=1):
                     yield
                 if st["S"].get(b) != (uid, j):
                     raise Hazard(f"softmax warp {w} ({uid},{j}) read S{b} = {st['S'].get(b)}")
-                yield  # the exponentials
+                yield  # the row maximum (all of S is now in registers)
                 if st["S"].get(b) != (uid, j):
                     raise Hazard("S overwritten while the softmax read it")
                 st["S_read"].setdefault(b, set()).add(w)
                 rescale = j > 0 and sim.rnd.random() < 0.3
-                if (sep_p or rescale) and it >= 1 and mistake != "no_pv_wait":
-                    while not sim.ready(f"o_done{(it - 1) & 1}", ((it - 1) >> 1) & 1, ((it - 1) >> 1) + 1):
-                        yield
+                pv_done = it == 0
+                done = [(uid, q, hf) for q in range(j) for hf in (0, 1)]
+                if rescale:
+                    # O~ first: PV(j - 1) done (S(j) may have finished before it)
+                    if mistake != "no_pv_wait":
+                        while not sim.ready(f"o_done{(it - 1) & 1}", ((it - 1) >> 1) & 1, ((it - 1) >> 1) + 1):
+                            yield
+                    pv_done = True
+                    if any(o != done for o in st["O"]):
+                        raise Hazard(f"rescale of ({uid},{j}) saw O = {st['O']}")
                 p_at = "sep" if sep_p else b
-                mine = st["P"].setdefault(p_at, {})
-                if mine.get(w) not in (None, "read"):
-                    raise Hazard(f"P ({uid},{j}) of warp {w} written over unread P {mine[w]}")
-                mine[w] = (uid, j)
-                if rescale and any(o != [(uid, q) for q in range(j)] for o in st["O"]):
-                    raise Hazard(f"rescale of ({uid},{j}) saw O = {st['O']}")
-                sim.bars[f"p_full{b}"].arrive((uid, j))
+                for hf, bar in ((0, "p_full"), (1, "p_hi")):
+                    yield  # the exponentials of this half
+                    if sep_p and not pv_done and mistake != "no_pv_wait":
+                        # P has a region of its own: PV(j - 1) must have read it
+                        while not sim.ready(f"o_done{(it - 1) & 1}", ((it - 1) >> 1) & 1, ((it - 1) >> 1) + 1):
+                            yield
+                        pv_done = True
+                    mine = st["P"].setdefault((p_at, hf), {})
+                    if mine.get(w) not in (None, "read"):
+                        raise Hazard(f"P ({uid},{j}) half {hf} of warp {w} written over unread P {mine[w]}")
+                    mine[w] = (uid, j)
+                    sim.bars[f"{bar}{b}"].arrive((uid, j))
                 it += 1
                 yield
             if ue > 0 and mistake != "no_stats_wait":
@@ -580,7 +601,7 @@ def run_one_tile(units, seed, nv, slots, sep_p, nb, mistake=None, warps=1):
             for _ in range(2):  # reads O and the statistics of its rows over a while
                 if st["stats"].get(w) != uid:
                     raise Hazard(f"epilogue warp {w} of {uid} read the statistics of {st['stats'].get(w)}")
-                if any(o != [(uid, q) for q in range(n)] for o in st["O"]):
+                if any(o != [(uid, q, hf) for q in range(n) for hf in (0, 1)] for o in st["O"]):
                     raise Hazard(f"epilogue of {uid} read O = {st['O']}")
                 yield
             if w == 0:
@@ -600,25 +621,27 @@ def run_one_tile(units, seed, nv, slots, sep_p, nb, mistake=None, warps=1):
             if c == 0:
                 if b in st["S"] and len(st["S_read"].get(b, ())) < warps:
                     raise Hazard(f"S ({uid},{j}) overwrote unread scores {st['S'][b]}")
-                if not sep_p and any(v != "read" for v in st["P"].get(b, {}).values()):
-                    raise Hazard(f"S ({uid},{j}) overwrote P {st['P'][b]} before PV read it")
-                if not sep_p:
-                    st["P"][b] = {}
+                for hf in (0, 1):
+                    if not sep_p and any(v != "read" for v in st["P"].get((b, hf), {}).values()):
+                        raise Hazard(f"S ({uid},{j}) overwrote P {st['P'][(b, hf)]} before PV read it")
+                    if not sep_p:
+                        st["P"][(b, hf)] = {}
             st["S"][b] = (uid, j) if c == nb - 1 else ("partial", uid, j)
             st["S_read"][b] = set()
         elif op == "PV":
-            uid, j, b, h, s = arg
+            uid, j, b, h, s, hf = arg
             p_at = "sep" if sep_p else b
-            quarters = st["P"].get(p_at, {})
+            quarters = st["P"].get((p_at, hf), {})
             if smem.get(f"v{s}") != (uid, j, h) or len(quarters) != warps or any(
                     v != (uid, j) for v in quarters.values()):
-                raise Hazard(f"PV ({uid},{j},{h}) read V {smem.get(f'v{s}')}, P {quarters}")
-            if j == 0:
+                raise Hazard(f"PV ({uid},{j},{h}) half {hf} read V {smem.get(f'v{s}')}, P {quarters}")
+            if j == 0 and hf == 0:
                 st["O"][h] = []
-            st["O"][h].append((uid, j))
-            st["v_read"][s] = True
+            st["O"][h].append((uid, j, hf))
+            if hf == 1:
+                st["v_read"][s] = True
             if h == nv - 1:
-                st["P"][p_at] = {w: "read" for w in quarters}
+                st["P"][(p_at, hf)] = {w: "read" for w in quarters}
 
     roles = [producer(), mma()] + [softmax(w) for w in range(warps)] + [
         epilogue(w) for w in range(warps)]
@@ -657,7 +680,7 @@ def test_one_tile_protocol_is_hazard_and_deadlock_free(cfg, warps):
 # inside the phase of the tile still landing.
 ONE_TILE_MISTAKES = {"no_s_buffer_wait": False, "no_v_slot_wait": True, "no_pv_wait": True,
                      "no_stats_wait": True, "no_o_free_wait": True, "no_k_box_wait": True,
-                     "k_box_release_early": True, "k_arm_early": True}
+                     "k_box_release_early": True, "k_arm_early": True, "no_p_hi_wait": True}
 
 
 @pytest.mark.parametrize("warps", [1, 4])
