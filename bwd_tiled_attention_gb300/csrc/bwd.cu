@@ -495,12 +495,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (c > 0 && !wait_or_abort(smem_u32(&sm.s_free), (c - 1) & 1, abort_flag, hdr))
                     return false;
                 tc_fence_after();
-                const uint32_t qaddr = smem_u32(sm.q[c & 1]);
+                const uint64_t da = make_sdesc_here(kaddr, 16, 1024);
+                const uint64_t db = make_sdesc_here(smem_u32(sm.q[c & 1]), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < DR / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem + Cfg::kColS, make_sdesc(kaddr + off, 16, 1024),
-                           make_sdesc(qaddr + off, 16, 1024), idS, kk > 0);
+                    mma_ss(tmem + Cfg::kColS, sdesc_add(da, off), sdesc_add(db, off), idS, kk > 0);
                 }
                 mma_commit(smem_u32(&sm.s_full));
                 return true;
@@ -535,11 +535,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 (!Cfg::kDqAliasesDp || cnt == 0 ||
                                  mbar_test_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
                                 tc_fence_after();
+                                const uint64_t da = make_sdesc_here(vaddr, 16, 1024);
+                                const uint64_t db = make_sdesc_here(doaddr, 16, 1024);
 #pragma unroll
                                 for (int kk = 0; kk < DR / 16; ++kk) {
                                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                    mma_ss(tmem + Cfg::kColDP, make_sdesc(vaddr + off, 16, 1024),
-                                           make_sdesc(doaddr + off, 16, 1024), idS, kk > 0);
+                                    mma_ss(tmem + Cfg::kColDP, sdesc_add(da, off), sdesc_add(db, off),
+                                           idS, kk > 0);
                                 }
                                 mma_commit(smem_u32(&sm.dp_full));
                                 dp_done = true;
@@ -551,12 +553,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 tc_fence_after();
                                 // P^T of query columns [64h, 64h+64) sits in TMEM
                                 // columns [64h, 64h+32)
+                                const uint64_t db = make_sdesc_here(doaddr, 16384, 1024);
 #pragma unroll
                                 for (int kk = 0; kk < kTile / 16; ++kk)
                                     mma_ts(tmem + Cfg::kColDV,
                                            tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
-                                           make_sdesc(doaddr + kk * 2048, 16384, 1024), idKV,
-                                           (s > 0 || kk > 0) ? 1u : 0u);
+                                           sdesc_add(db, kk * 2048), idKV, (s > 0 || kk > 0) ? 1u : 0u);
                                 mma_commit(smem_u32(&sm.s_free));
                                 dv_done = true;
                                 continue;
@@ -584,12 +586,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  mbar_test_wait(smem_u32(&sm.dq_free), (cnt - 1) & 1))) {
                                 tc_fence_after();
                                 // dQ = dS K_j  (A = dS^T in shared memory read as MN-major)
+                                const uint64_t da = make_sdesc_here(dsaddr, 16384, 1024);
+                                const uint64_t db = make_sdesc_here(kaddr, 16384, 1024);
 #pragma unroll
                                 for (int kk = 0; kk < kTile / 16; ++kk)
-                                    mma_ss(tmem + Cfg::kColDQ,
-                                           make_sdesc(dsaddr + kk * 2048, 16384, 1024),
-                                           make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ,
-                                           kk > 0);
+                                    mma_ss(tmem + Cfg::kColDQ, sdesc_add(da, kk * 2048),
+                                           sdesc_add(db, kk * 2048), idDQ, kk > 0);
                                 // committed at once: a commit tracks every MMA issued before
                                 // it, and the drain must not wait for later ones
                                 mma_commit(smem_u32(&sm.dq_full));
@@ -601,12 +603,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                ((cnt + 1) >> 1) & 1) &&
                                 mbar_test_wait(smem_u32(&sm.s_free), cnt & 1)) {
                                 tc_fence_after();
-                                const uint32_t qn = smem_u32(sm.q[(cnt + 1) & 1]);
+                                const uint64_t da = make_sdesc_here(kaddr, 16, 1024);
+                                const uint64_t db = make_sdesc_here(smem_u32(sm.q[(cnt + 1) & 1]), 16, 1024);
 #pragma unroll
                                 for (int kk = 0; kk < DR / 16; ++kk) {
                                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                    mma_ss(tmem + Cfg::kColS, make_sdesc(kaddr + off, 16, 1024),
-                                           make_sdesc(qn + off, 16, 1024), idS, kk > 0);
+                                    mma_ss(tmem + Cfg::kColS, sdesc_add(da, off), sdesc_add(db, off),
+                                           idS, kk > 0);
                                 }
                                 mma_commit(smem_u32(&sm.s_full));
                                 s_done = true;
@@ -614,12 +617,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             }
                             if (!k_done && q_done) {
                                 // dK_j += dS^T Q  (A = dS^T in shared memory, K-major)
+                                const uint64_t da = make_sdesc_here(dsaddr, 16, 1024);
+                                const uint64_t db = make_sdesc_here(qaddr, 16384, 1024);
 #pragma unroll
                                 for (int kk = 0; kk < kTile / 16; ++kk) {
                                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                    mma_ss(tmem + Cfg::kColDK, make_sdesc(dsaddr + off, 16, 1024),
-                                           make_sdesc(qaddr + kk * 2048, 16384, 1024), idKV,
-                                           (s > 0 || kk > 0) ? 1u : 0u);
+                                    mma_ss(tmem + Cfg::kColDK, sdesc_add(da, off), sdesc_add(db, kk * 2048),
+                                           idKV, (s > 0 || kk > 0) ? 1u : 0u);
                                 }
                                 mma_commit(smem_u32(&sm.ds_free));       // dS read by dQ and dK
                                 mma_commit(smem_u32(&sm.q_empty[st]));   // Q(c) read by S(c), dK

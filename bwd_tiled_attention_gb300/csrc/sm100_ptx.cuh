@@ -240,6 +240,21 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Descriptor of (saddr + off) from that of saddr: the start-address field holds
+// saddr >> 4 in 14 bits and shared-memory addresses stay below 256 KB, so
+// adding off >> 4 never carries into the next field (off a multiple of 16).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t off) {
+    return desc + (uint64_t)(off >> 4);
+}
+
+// make_sdesc built where it is used: the empty asm keeps the compiler from
+// hoisting the (loop-invariant) descriptor out of a thread's main loop and
+// holding it, 64 bits at a time, in registers the issuing thread lacks.
+__device__ __forceinline__ uint64_t make_sdesc_here(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    asm volatile("" : "+r"(saddr));
+    return make_sdesc(saddr, lbo, sbo);
+}
+
 // ---------------------------------------------------------------- tcgen05: TMEM <-> registers
 
 // 32 lanes x 32 bits, 32 consecutive columns per thread.
