@@ -1230,10 +1230,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 for (int cc = 0; cc < C; ++cc) {
                     const uint32_t a = acquire();
                     if (!a) return false;
+                    const uint64_t da = make_sdesc_here(abase + cc * 16384, 16, 1024);
+                    const uint64_t db = make_sdesc_here(a, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tmem + col, make_sdesc(abase + cc * 16384 + kk * 32, 16, 1024),
-                               make_sdesc(a + kk * 32, 16, 1024), idS, (cc | kk) > 0);
+                        mma_ss(tmem + col, sdesc_add(da, kk * 32), sdesc_add(db, kk * 32), idS,
+                               (cc | kk) > 0);
                     release();
                 }
                 return true;
@@ -1266,10 +1268,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         tc_fence_after();
                         for (int cc = 0; cc < C && ok;) {
                             const int n = acc_chunks(cc, [&](uint32_t col, uint32_t a, bool n128) {
+                                const uint64_t db = make_sdesc_here(a, 16384, 1024);
 #pragma unroll
                                 for (int kk = 0; kk < kTile / 16; ++kk)
                                     mma_ts(tmem + col, tmem + b * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
-                                           make_sdesc(a + kk * 2048, 16384, 1024), n128 ? idN2 : idN,
+                                           sdesc_add(db, kk * 2048), n128 ? idN2 : idN,
                                            (s > 1 || kk > 0) ? 1u : 0u);
                             });
                             ok = n > 0;
@@ -1299,11 +1302,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     // dK += dS^T Q_i, 64 columns of Q per chunk (A = dS^T, K-major)
                     for (int cc = 0; cc < C && ok;) {
                         const int n = acc_chunks(cc, [&](uint32_t col, uint32_t a, bool n128) {
+                            const uint64_t da = make_sdesc_here(dsaddr, 16, 1024);
+                            const uint64_t db = make_sdesc_here(a, 16384, 1024);
 #pragma unroll
                             for (int kk = 0; kk < kTile / 16; ++kk)
-                                mma_ss(tmem + col,
-                                       make_sdesc(dsaddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                                       make_sdesc(a + kk * 2048, 16384, 1024), n128 ? idN2 : idN,
+                                mma_ss(tmem + col, sdesc_add(da, (kk >> 2) * 16384 + (kk & 3) * 32),
+                                       sdesc_add(db, kk * 2048), n128 ? idN2 : idN,
                                        (s > 0 || kk > 0) ? 1u : 0u);
                         });
                         ok = n > 0;
@@ -1311,10 +1315,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     }
                     if (!ok) break;
                     // dQ = dS K_j into [0, D): S^T and dP^T have been read
+                    {
+                        const uint64_t da = make_sdesc_here(dsaddr, 16384, 1024);
+                        const uint64_t db = make_sdesc_here(kaddr, 16384, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ss(tmem, make_sdesc(dsaddr + kk * 2048, 16384, 1024),
-                               make_sdesc(kaddr + kk * 2048, 16384, 1024), idDQ, kk > 0);
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ss(tmem, sdesc_add(da, kk * 2048), sdesc_add(db, kk * 2048), idDQ,
+                                   kk > 0);
+                    }
                     mma_commit(smem_u32(&sm.dq_full));
                     if (!(ok = expect(pend_s[0], smem_u32(&sm.dq_free[0]), c & 1))) break;
                     ok = expect(pend_s[1], smem_u32(&sm.dq_free[1]), c & 1);

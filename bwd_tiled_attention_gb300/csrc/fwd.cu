@@ -477,12 +477,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                                          abort_flag, hdr)))
                                     break;
                                 tc_fence_after();
-                                const uint32_t qa = smem_u32(sm.q[0]), kb = smem_u32(sm.k[0]);
+                                const uint64_t da = make_sdesc_here(smem_u32(sm.q[0]), 16, 1024);
+                                const uint64_t db = make_sdesc_here(smem_u32(sm.k[0]), 16, 1024);
 #pragma unroll
                                 for (int kk = 0; kk < D / 16; ++kk) {
                                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                    mma_ss(tmem + b * 128, make_sdesc(qa + off, 16, 1024),
-                                           make_sdesc(kb + off, 16, 1024), idS, kk > 0);
+                                    mma_ss(tmem + b * 128, sdesc_add(da, off), sdesc_add(db, off), idS,
+                                           kk > 0);
                                     // K's box kk / 4 is read once its four MMAs are done
                                     if ((kk & 3) == 3) mma_commit(smem_u32(&sm.k_empty[kk >> 2]));
                                 }
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                     break;
                                 if (jp < n) {
                                     tc_fence_after();
-                                    const uint32_t vb = smem_u32(sm.v[slot]);
+                                    const uint64_t db = make_sdesc_here(smem_u32(sm.v[slot]), 16384, 1024);
                                     // the first chunk starts on keys [0, 64) of P and waits
                                     // for [64, 128) halfway
 #pragma unroll
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                         }
                                         mma_ts(tmem + 256 + h * Cfg::kVChunk,
                                                tmem + (Cfg::kSepP ? Cfg::kPCol : b * 128) + kk * 8,
-                                               make_sdesc(vb + kk * 2048, 16384, 1024), idPV,
+                                               sdesc_add(db, kk * 2048), idPV,
                                                (jp > 0 || kk > 0) ? 1u : 0u);
                                     }
                                     if (!ok) break;
