@@ -530,6 +530,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     {
                         bool dp_done = false, dv_done = false;
                         const uint64_t t_start = globaltimer();
+                        uint32_t spins = 0;  // the timer and abort flag every 64 polls
                         while (!(dp_done && dv_done)) {
                             if (!dp_done &&
                                 (!Cfg::kDqAliasesDp || cnt == 0 ||
@@ -563,7 +564,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 dv_done = true;
                                 continue;
                             }
-                            if (*abort_flag || globaltimer() - t_start > kSpinLimitNs) {
+                            if ((++spins & 63u) == 0 &&
+                                (*abort_flag || globaltimer() - t_start > kSpinLimitNs)) {
                                 raise_abort(abort_flag, hdr, kErrTimeout);
                                 ok = false;
                                 break;
@@ -580,6 +582,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     {
                         bool s_done = s + 1 >= x.ns, q_done = false, k_done = false;
                         const uint64_t t_start = globaltimer();
+                        uint32_t spins = 0;  // the timer and abort flag every 64 polls
                         while (!(s_done && q_done && k_done)) {
                             if (!q_done && mbar_test_wait(smem_u32(&sm.ds_ready), cnt & 1) &&
                                 (Cfg::kDqAliasesDp || cnt == 0 ||
@@ -630,7 +633,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 k_done = true;
                                 continue;
                             }
-                            if (*abort_flag || globaltimer() - t_start > kSpinLimitNs) {
+                            if ((++spins & 63u) == 0 &&
+                                (*abort_flag || globaltimer() - t_start > kSpinLimitNs)) {
                                 raise_abort(abort_flag, hdr, kErrTimeout);
                                 ok = false;
                                 break;
