@@ -88,8 +88,8 @@ struct BwdSmem {
     alignas(1024) uint8_t dout[BwdCfg<D>::kTileBytes];   // dO (1 stage)
     alignas(1024) uint8_t ds[kTile * kTile * 2];         // dS^T: 128 key rows x 128 query cols
     alignas(1024) uint8_t stage[2][kTile * 128];         // dQ staging: 2 slots of 128 rows x 128 B
-    alignas(16) float lse2[2][kTile];                    // LSE * log2(e) of the Q stage's rows
-    alignas(16) float dd[2][kTile];                      // D of the Q stage's rows
+    alignas(16) float lse2[2][kTile];                    // -LSE * log2(e) of the Q stage's rows
+    alignas(16) float dd[2][kTile];                      // -D of the Q stage's rows
     alignas(8) uint64_t sched_full[2], sched_empty[2];
     uint64_t kv_full, kv_empty;
     uint64_t q_full[2], q_empty[2], do_full, do_empty;
@@ -287,6 +287,32 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* l
     }
 }
 
+// As p_chunk, for a row of negated LSE2 values: S^T * c - LSE2 is one packed
+// fp32-pair FMA per two columns.
+template <bool MASK>
+__device__ __forceinline__ void p_chunk_f2(const uint32_t (&sv)[32], const float* nl2, uint64_t cc,
+                                           int lo, int hi, int xb, uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int e4 = 0; e4 < 8; ++e4) {
+        const ulonglong2 lv = reinterpret_cast<const ulonglong2*>(nl2)[e4];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int e = e4 * 2 + h2;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), cc,
+                             h2 ? lv.y : lv.x),
+                      x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (MASK) {
+                const int y0 = xb + 2 * e, y1 = y0 + 1;
+                p0 = (y0 >= lo && y0 < hi) ? p0 : 0.f;
+                p1 = (y1 >= lo && y1 < hi) ? p1 : 0.f;
+            }
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+    }
+}
+
 // D: the tile layout (64 or 128 columns); DR: the head dimension in memory.
 // DR = 96 runs on 128-column tiles: the TMA boxes past column 96 read zeros.
 // S and dP contract over the first 96 columns only (6 MMAs of K = 16).  dV, dK
@@ -426,8 +452,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         l2 = p.lse[at] * kLog2e;
                         dv = p.D[at];
                     }
-                    sm.lse2[st][rr] = l2;
-                    sm.dd[st][rr] = dv;
+                    sm.lse2[st][rr] = -l2;
+                    sm.dd[st][rr] = -dv;
                 }
                 mbar_arrive(qbar);
             }
@@ -672,6 +698,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t dp_addr = tmem + lane_off + Cfg::kColDP;
         uint8_t* ds_row = sm.ds + hc * 16384 + rk * 128;  // this half's 64-column block
         const int sw = rk & 7;
+        const uint64_t cc2 = f2_pack(p.scale_log2, p.scale_log2);
         int sched_it = 0, cnt = 0;
         bool ok = true;
         while (ok) {
@@ -721,9 +748,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     for (int h = 0; h < 2; ++h) {
                         const int xb = hc * 64 + h * 32;  // first query column of the chunk
                         if (full)
-                            p_chunk<false>(sv[h], l2 + h * 32, p.scale_log2, lo, hi, xb, pk[h]);
+                            p_chunk_f2<false>(sv[h], l2 + h * 32, cc2, lo, hi, xb, pk[h]);
                         else
-                            p_chunk<true>(sv[h], l2 + h * 32, p.scale_log2, lo, hi, xb, pk[h]);
+                            p_chunk_f2<true>(sv[h], l2 + h * 32, cc2, lo, hi, xb, pk[h]);
                         // into this half's own S^T columns, which this warp has
                         // already read (the other half's are still being read)
                         tmem_st16(s_addr + hc * 64 + h * 16, pk[h]);
@@ -750,18 +777,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         uint32_t out[16];
 #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 dvv = reinterpret_cast<const float4*>(dd + h * 32)[e4];
-                            const float da[4] = {dvv.x, dvv.y, dvv.z, dvv.w};
+                            const ulonglong2 nd = reinterpret_cast<const ulonglong2*>(dd + h * 32)[e4];
 #pragma unroll
                             for (int h2 = 0; h2 < 2; ++h2) {
                                 const int e = e4 * 2 + h2;
-                                __nv_bfloat162 pp =
-                                    *reinterpret_cast<const __nv_bfloat162*>(&pk[h][e]);
-                                const float2 pf = __bfloat1622float2(pp);
-                                const float d0 =
-                                    pf.x * (__uint_as_float(dv[h][2 * e]) - da[2 * h2]);
-                                const float d1 =
-                                    pf.y * (__uint_as_float(dv[h][2 * e + 1]) - da[2 * h2 + 1]);
+                                const uint32_t pp = pk[h][e];
+                                const uint64_t pf = f2_pack(__uint_as_float(pp << 16),
+                                                            __uint_as_float(pp & 0xffff0000u));
+                                const uint64_t t = f2_add(f2_pack(__uint_as_float(dv[h][2 * e]),
+                                                                  __uint_as_float(dv[h][2 * e + 1])),
+                                                          h2 ? nd.y : nd.x);
+                                float d0, d1;
+                                f2_unpack(f2_mul(t, pf), d0, d1);
                                 out[e] = pack_bf16x2(d0, d1);
                             }
                         }
