@@ -264,33 +264,11 @@ __device__ bool sem_wait(const int* sem, int target, const WsHeader* hdr) {
 }
 
 // P^T for one 32-column chunk of a key row: exp2(S^T * c - LSE2) as packed
-// bf16 pairs; with MASK, columns outside [lo, hi) are zero.
+// bf16 pairs; with MASK, columns outside [lo, hi) are zero.  nl2 holds the
+// chunk's LSE2 values negated and cc is c in both halves of an fp32 pair, so
+// the scaling is one packed FMA per two columns.
 template <bool MASK>
-__device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* l2, float c2,
-                                        int lo, int hi, int xb, uint32_t (&pk)[16]) {
-#pragma unroll
-    for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 lv = reinterpret_cast<const float4*>(l2)[e4];
-        const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int e = e4 * 2 + h2;
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), c2, -la[2 * h2]));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), c2, -la[2 * h2 + 1]));
-            if (MASK) {
-                const int x0 = xb + 2 * e, x1 = x0 + 1;
-                p0 = (x0 >= lo && x0 < hi) ? p0 : 0.f;
-                p1 = (x1 >= lo && x1 < hi) ? p1 : 0.f;
-            }
-            pk[e] = pack_bf16x2(p0, p1);
-        }
-    }
-}
-
-// As p_chunk, for a row of negated LSE2 values: S^T * c - LSE2 is one packed
-// fp32-pair FMA per two columns.
-template <bool MASK>
-__device__ __forceinline__ void p_chunk_f2(const uint32_t (&sv)[32], const float* nl2, uint64_t cc,
+__device__ __forceinline__ void p_chunk(const uint32_t (&sv)[32], const float* nl2, uint64_t cc,
                                            int lo, int hi, int xb, uint32_t (&pk)[16]) {
 #pragma unroll
     for (int e4 = 0; e4 < 8; ++e4) {
@@ -748,9 +726,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     for (int h = 0; h < 2; ++h) {
                         const int xb = hc * 64 + h * 32;  // first query column of the chunk
                         if (full)
-                            p_chunk_f2<false>(sv[h], l2 + h * 32, cc2, lo, hi, xb, pk[h]);
+                            p_chunk<false>(sv[h], l2 + h * 32, cc2, lo, hi, xb, pk[h]);
                         else
-                            p_chunk_f2<true>(sv[h], l2 + h * 32, cc2, lo, hi, xb, pk[h]);
+                            p_chunk<true>(sv[h], l2 + h * 32, cc2, lo, hi, xb, pk[h]);
                         // into this half's own S^T columns, which this warp has
                         // already read (the other half's are still being read)
                         tmem_st16(s_addr + hc * 64 + h * 16, pk[h]);
@@ -1040,8 +1018,8 @@ struct WideSmem {
     // dS^T (two 64-column boxes, 128B-swizzled); once dK and dQ have read it,
     // the staging of the dQ merge (two 32-column fp32 slots)
     alignas(1024) uint8_t ds[kTile * kTile * 2];
-    alignas(16) float lse2[2][kTile];  // LSE * log2(e) of the step's query rows
-    alignas(16) float dd[2][kTile];    // D of the step's query rows
+    alignas(16) float lse2[2][kTile];  // -LSE * log2(e) of the step's query rows
+    alignas(16) float dd[2][kTile];    // -D of the step's query rows
     alignas(8) uint64_t sched_full[2], sched_empty[2];
     uint64_t kv_full, kv_empty;
     uint64_t slot_full[WideCfg<D>::kSlots], slot_free[WideCfg<D>::kSlots];
@@ -1466,14 +1444,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 tc_fence_before();  // (the next arrival orders these reads before dK / dV)
             };
 
+            const uint64_t cc2 = f2_pack(p.scale_log2, p.scale_log2);
             for (int pass = 0; pass < 2 && ok; ++pass) {
                 float nl2 = 0.f, ndd = 0.f;
                 if (x.ns > 0) fetch_rows(walk_tile<KV>(x, 0, p.deterministic, p.causal), nl2, ndd);
                 for (int s = 0; s < x.ns; ++s) {
                     const int i = walk_tile<KV>(x, s, p.deterministic, p.causal);
                     const int rb = rs++ & 1;  // row buffer: its readers of two steps ago are past
-                    sm.lse2[rb][ct] = nl2;    // the named barrier of the previous step
-                    sm.dd[rb][ct] = ndd;
+                    sm.lse2[rb][ct] = -nl2;   // the named barrier of the previous step
+                    sm.dd[rb][ct] = -ndd;
                     // (the wait's block-wide vote also publishes the rows)
                     const uint32_t full_bar =
                         pass == 0 ? smem_u32(&sm.s_full[(c1 + s) & 1]) : smem_u32(&sm.sdp_full);
@@ -1499,9 +1478,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         for (int qc = 0; qc < 4; ++qc) {
                             uint32_t pk[16];
                             if (full)
-                                p_chunk<false>(sv[qc], sm.lse2[rb] + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                                p_chunk<false>(sv[qc], sm.lse2[rb] + qc * 32, cc2, lo, hi, qc * 32, pk);
                             else
-                                p_chunk<true>(sv[qc], sm.lse2[rb] + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                                p_chunk<true>(sv[qc], sm.lse2[rb] + qc * 32, cc2, lo, hi, qc * 32, pk);
                             tmem_st16(sb + (qc >> 1) * 64 + (qc & 1) * 16, pk);
                         }
                         tmem_st_wait();
@@ -1522,17 +1501,20 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         tmem_ld_wait();
                         uint32_t pk[16];
                         if (full)
-                            p_chunk<false>(sv, sm.lse2[rb] + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                            p_chunk<false>(sv, sm.lse2[rb] + qc * 32, cc2, lo, hi, qc * 32, pk);
                         else
-                            p_chunk<true>(sv, sm.lse2[rb] + qc * 32, p.scale_log2, lo, hi, qc * 32, pk);
+                            p_chunk<true>(sv, sm.lse2[rb] + qc * 32, cc2, lo, hi, qc * 32, pk);
                         uint32_t out[16];
+                        const uint64_t* nd = reinterpret_cast<const uint64_t*>(sm.dd[rb] + qc * 32);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const float2 pf =
-                                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[e]));
-                            const float d0 = sm.dd[rb][qc * 32 + 2 * e], d1 = sm.dd[rb][qc * 32 + 2 * e + 1];
-                            out[e] = pack_bf16x2(pf.x * (__uint_as_float(dv[2 * e]) - d0),
-                                                 pf.y * (__uint_as_float(dv[2 * e + 1]) - d1));
+                            const uint64_t pf = f2_pack(__uint_as_float(pk[e] << 16),
+                                                        __uint_as_float(pk[e] & 0xffff0000u));
+                            const uint64_t t = f2_add(
+                                f2_pack(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd[e]);
+                            float d0, d1;
+                            f2_unpack(f2_mul(t, pf), d0, d1);
+                            out[e] = pack_bf16x2(d0, d1);
                         }
                         // 32 query columns = 4 chunks of 16 bytes of half (qc >> 1)'s block
 #pragma unroll
