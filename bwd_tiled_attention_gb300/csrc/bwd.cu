@@ -1639,7 +1639,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
 // D = rowsum(dO * O) per (token, head); zero the dQ accumulator row and the
 // semaphores.  Each lane takes 8 elements (16-byte loads), D/8 lanes per row,
-// so a warp covers 32/(D/8) rows per pass.
+// so a warp covers 32/(D/8) rows per grid stride; it takes two strides per
+// pass, with the loads of both in flight before either is used (the kernel is
+// bound by HBM, and more bytes in flight per SM bring it closer).
 template <int D, bool O_FP32>  // D: the head dimension in memory (64, 96 or 128)
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const void* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
@@ -1654,45 +1656,60 @@ __global__ void __launch_bounds__(256)
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR, l = lane % LPR;
-    for (long long r0 = warp_g * RPW; r0 < rows; r0 += nwarps * RPW) {
-        const long long r = r0 + sub;
-        const bool valid = r < rows;
-        float acc = 0.f;
-        if (valid && l * 8 < D) {
-            const size_t base = (size_t)r * D + (size_t)l * 8;
-            const uint4 dv = *reinterpret_cast<const uint4*>(dout + base);
-            const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
-            float ov[8];
-            if (O_FP32) {
-                const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base);
-                const float4 b =
-                    *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base + 4);
-                ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w;
-                ov[4] = b.x; ov[5] = b.y; ov[6] = b.z; ov[7] = b.w;
-            } else {
-                const uint4 ow = *reinterpret_cast<const uint4*>(
-                    static_cast<const __nv_bfloat16*>(o) + base);
-                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ow);
+    // two rows per lane and pass, both rows' loads issued before either is used
+    for (long long r0 = warp_g * RPW; r0 < rows; r0 += 2 * nwarps * RPW) {
+        long long r[2];
+        bool valid[2];
+        uint4 dv[2], ow[2];
+        float4 fa[2], fb[2];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(o2[e]);
-                    ov[2 * e] = f.x;
-                    ov[2 * e + 1] = f.y;
+        for (int u = 0; u < 2; ++u) {
+            r[u] = r0 + (long long)u * nwarps * RPW + sub;
+            valid[u] = r[u] < rows && l * 8 < D;
+            if (valid[u]) {
+                const size_t base = (size_t)r[u] * D + (size_t)l * 8;
+                dv[u] = *reinterpret_cast<const uint4*>(dout + base);
+                if (O_FP32) {
+                    fa[u] = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base);
+                    fb[u] = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base + 4);
+                } else {
+                    ow[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(o) + base);
                 }
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(d2[e]);
-                acc = fmaf(ov[2 * e], f.x, acc);
-                acc = fmaf(ov[2 * e + 1], f.y, acc);
-            }
-            float4* z = reinterpret_cast<float4*>(dq_acc + base);
-            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (valid && l == 0) Dout[(size_t)(r % Hq) * T + (size_t)(r / Hq)] = acc;
+        for (int u = 0; u < 2; ++u) {
+            float acc = 0.f;
+            if (valid[u]) {
+                const size_t base = (size_t)r[u] * D + (size_t)l * 8;
+                const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv[u]);
+                float ov[8];
+                if (O_FP32) {
+                    ov[0] = fa[u].x; ov[1] = fa[u].y; ov[2] = fa[u].z; ov[3] = fa[u].w;
+                    ov[4] = fb[u].x; ov[5] = fb[u].y; ov[6] = fb[u].z; ov[7] = fb[u].w;
+                } else {
+                    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ow[u]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(o2[e]);
+                        ov[2 * e] = f.x;
+                        ov[2 * e + 1] = f.y;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(d2[e]);
+                    acc = fmaf(ov[2 * e], f.x, acc);
+                    acc = fmaf(ov[2 * e + 1], f.y, acc);
+                }
+                float4* z = reinterpret_cast<float4*>(dq_acc + base);
+                z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (valid[u] && l == 0) Dout[(size_t)(r[u] % Hq) * T + (size_t)(r[u] / Hq)] = acc;
+        }
     }
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     for (long long si = tid; si < n_sems; si += (long long)gridDim.x * blockDim.x) sems[si] = 0;
@@ -1713,8 +1730,23 @@ __global__ void __launch_bounds__(256)
     const long long nq = (long long)Tq * Hq * V;
     const long long nkv = dk_acc ? (long long)Tk * Hkv * V : 0;
     const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < nq + 2 * nkv;
-         e += stride) {
+    long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    // dQ, four groups per thread and pass, all four loads issued first
+    for (; e + 3 * stride < nq; e += 4 * stride) {
+        float4 a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = reinterpret_cast<const float4*>(dq_acc)[e + u * stride];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float4 r = make_float4(a[u].x * scale, a[u].y * scale, a[u].z * scale, a[u].w * scale);
+            if (F32)
+                reinterpret_cast<float4*>(dq)[e + u * stride] = r;
+            else
+                reinterpret_cast<uint2*>(dq)[e + u * stride] =
+                    make_uint2(pack_bf16x2(r.x, r.y), pack_bf16x2(r.z, r.w));
+        }
+    }
+    for (; e < nq + 2 * nkv; e += stride) {
         float4 r;
         void* out;
         long long oi;
