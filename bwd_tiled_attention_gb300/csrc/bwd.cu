@@ -93,7 +93,7 @@ struct BwdSmem {
     alignas(8) uint64_t sched_full[2], sched_empty[2];
     uint64_t kv_full, kv_empty;
     uint64_t q_full[2], q_empty[2], do_full, do_empty;
-    uint64_t s_full, dp_full, p_ready, ds_ready, s_free, ds_free, dq_full, dq_free;
+    uint64_t s_full, dp_full, p_ready, ds_ready, s_free, dq_full, dq_free;
     uint64_t dkv_full, dkv_free, drain;
     int2 sched[2];
     uint32_t tmem_base;
@@ -335,7 +335,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(smem_u32(&sm.p_ready), 8);
         mbar_init(smem_u32(&sm.ds_ready), 8);
         mbar_init(smem_u32(&sm.s_free), 1);
-        mbar_init(smem_u32(&sm.ds_free), 1);
         mbar_init(smem_u32(&sm.dq_full), 1);
         mbar_init(smem_u32(&sm.dq_free), 4);
         mbar_init(smem_u32(&sm.dkv_full), 1);
@@ -632,7 +631,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                     mma_ss(tmem + Cfg::kColDK, sdesc_add(da, off), sdesc_add(db, kk * 2048),
                                            idKV, (s > 0 || kk > 0) ? 1u : 0u);
                                 }
-                                mma_commit(smem_u32(&sm.ds_free));       // dS read by dQ and dK
                                 mma_commit(smem_u32(&sm.q_empty[st]));   // Q(c) read by S(c), dK
                                 k_done = true;
                                 continue;
@@ -739,10 +737,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sm.p_ready));
                 // dS^T = P^T * (dP^T - D), bf16, swizzled rows of the dS^T tile
+                // dp_full(c) also means dQ(c-1) and dK(c-1), the readers of the
+                // last dS^T, are done: the MMA thread issued them before dP(c),
+                // and a commit tracks every MMA issued before it
                 if (!(ok = warp_wait(smem_u32(&sm.dp_full), cnt & 1, abort_flag, hdr))) break;
-                if (cnt > 0 &&
-                    !(ok = warp_wait(smem_u32(&sm.ds_free), (cnt - 1) & 1, abort_flag, hdr)))
-                    break;
                 tc_fence_after();
                 const float* dd = sm.dd[st] + hc * 64;
                 {

@@ -40,7 +40,7 @@ def run_bwd(units, seed, alias, mistake=None, warps=1):
     parts = 2 * warps  # compute actors: query-column half x key-row quarter
     sim = Sim([(n,) for n in units], seed, consumers=3 + parts + warps - 1)
     for name in ("kv_full", "kv_empty", "do_full", "do_empty", "s_full", "dp_full", "s_free",
-                 "ds_free", "dq_full", "dkv_full"):
+                 "dq_full", "dkv_full"):
         sim.bar(name)
     for name in ("p_ready", "ds_ready"):
         sim.bar(name, parts)
@@ -108,6 +108,7 @@ def run_bwd(units, seed, alias, mistake=None, warps=1):
 
     def mma():
         it_sched = it_unit = cnt = 0
+        held_dk = None  # the dk_after_next_dp mistake: dK(c) held back past dP(c+1)
         while True:
             unit = yield from sim.take(it_sched)
             it_sched += 1
@@ -132,6 +133,9 @@ def run_bwd(units, seed, alias, mistake=None, warps=1):
                     if not dp_done and (not alias or cnt == 0 or mistake == "no_dq_free_wait"
                                         or sim.ready("dq_free", (cnt - 1) & 1, cnt)):
                         sim.pipe += [("dP", (uid, s)), ("commit", "dp_full")]
+                        if held_dk:
+                            sim.pipe += held_dk
+                            held_dk = None
                         dp_done = True
                         continue
                     if not dv_done and sim.ready("p_ready", cnt & 1, cnt + 1) and (
@@ -157,8 +161,11 @@ def run_bwd(units, seed, alias, mistake=None, warps=1):
                         s_done = True
                         continue
                     if not k_done and q_done:
-                        sim.pipe += [("dK", (uid, s, q)), ("commit", "ds_free"),
-                                     ("q_read", q), ("commit", f"q_empty{q}")]
+                        ops = [("dK", (uid, s, q)), ("q_read", q), ("commit", f"q_empty{q}")]
+                        if mistake == "dk_after_next_dp" and s + 1 < ni:
+                            held_dk = ops
+                        else:
+                            sim.pipe += ops
                         k_done = True
                         continue
                     yield
@@ -191,11 +198,11 @@ def run_bwd(units, seed, alias, mistake=None, warps=1):
                 yield  # P^T = exp2(S^T - LSE)
                 st["S"][pt] = ("P", uid, s)
                 sim.bars["p_ready"].arrive((uid, s))
+                # dp_full(c) also covers dQ(c-1) and dK(c-1), the readers of the
+                # last dS^T: the issuer puts both ahead of dP(c) on the in-order
+                # pipe, so the kernel has no barrier of its own for them
                 while not sim.ready("dp_full", cnt & 1, cnt + 1):
                     yield
-                if cnt > 0 and mistake != "no_ds_free_wait":
-                    while not sim.ready("ds_free", (cnt - 1) & 1, cnt):
-                        yield
                 if st["dP"] != (uid, s) or st["rows"].get(q) != (uid, s):
                     raise Hazard(f"compute {pt} ({uid},{s}) read dP {st['dP']}")
                 # this part's slice of the last complete dS^T tile must have been
@@ -326,13 +333,14 @@ def test_bwd_protocol_is_hazard_and_deadlock_free(alias, warps):
 # others (False), which the kernel keeps all the same:
 # - no_s_free_wait: with an in-order tensor pipe, S(c+1) runs after dV(c),
 #   the last reader of P^T(c), which was issued before it.
-# - no_ds_free_wait: dS(c) is written after dP(c) has run, and dP(c) was
-#   issued after dQ(c-1) and dK(c-1), the readers of dS(c-1).
+# - dk_after_next_dp (caught): dK(c) held back until after dP(c+1).  The
+#   compute warps write dS(c+1) once dp_full(c+1) completes, and take that as
+#   proof that dK(c) has read dS(c); this issue order would break it.
 # no_empty_unit_dkv_wait is the wait at the end of a unit no query sees: the
 # model found it missing (two such units in a row put dkv_full two phases
 # ahead of the epilogue warps).
 BWD_MISTAKES = {"no_q_empty_wait": True, "no_do_empty_wait": True, "no_dq_free_wait": True,
-                "no_dkv_free_wait": True, "no_ds_free_wait": False, "no_s_free_wait": False,
+                "no_dkv_free_wait": True, "dk_after_next_dp": True, "no_s_free_wait": False,
                 "no_empty_unit_dkv_wait": True}
 
 
